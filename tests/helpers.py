@@ -1,0 +1,76 @@
+"""Shared test plumbing: oracle-side arrays for a workload (uses ``oracle``)."""
+from __future__ import annotations
+
+import dataclasses
+import json
+import os
+
+import numpy as np
+
+import oracle
+from workloads import Workload, generate
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+# bf16 bit patterns used to poison memory the kernels must not use.
+POISON_BITS = np.uint16(0x4280)      # 64.0: large but finite
+CANARY_BITS = np.uint16(0x7F7F)      # 3.39e38: finite, never a legal output
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+@dataclasses.dataclass
+class Case:
+    w: Workload
+    inputs: object
+    q_bits: np.ndarray        # [T, NQ, HD] uint16
+    k_new_bits: np.ndarray    # [T, NKV, HD]
+    v_new_bits: np.ndarray
+    k_cache_bits: np.ndarray  # [B, NKV, P, S, HD] striped, holes = POISON_BITS
+    v_cache_bits: np.ndarray
+
+    def f64(self, name: str) -> np.ndarray:
+        return oracle.bits_to_f64(getattr(self, name + "_bits"))
+
+    def oracle_full(self, threads: int = 1):
+        w = self.w
+        return oracle.attend_ref(self.f64("q"), self.f64("k_new"), self.f64("v_new"),
+                                 self.f64("k_cache"), self.f64("v_cache"), w.cache_lens,
+                                 w.chunk_lens, w.chunk, w.scale, threads=threads)
+
+    def oracle_rows(self, samples):
+        w = self.w
+        return oracle.attend_rows_ref(self.q_bits, self.k_new_bits, self.v_new_bits,
+                                      self.k_cache_bits, self.v_cache_bits, w.cache_lens,
+                                      w.chunk_lens, w.chunk, w.scale, samples)
+
+
+def make_case(w: Workload, hole_bits=POISON_BITS) -> Case:
+    inp = generate(w)
+    kc = oracle.build_striped_cache([oracle.bf16_bits(x) for x in inp.k_cache], w.num_kv_heads,
+                                    w.shards, w.shard_capacity, w.head_dim, hole_bits)
+    vc = oracle.build_striped_cache([oracle.bf16_bits(x) for x in inp.v_cache], w.num_kv_heads,
+                                    w.shards, w.shard_capacity, w.head_dim, hole_bits)
+    return Case(w=w, inputs=inp, q_bits=oracle.bf16_bits(inp.q),
+                k_new_bits=oracle.bf16_bits(inp.k_new), v_new_bits=oracle.bf16_bits(inp.v_new),
+                k_cache_bits=kc, v_cache_bits=vc)
+
+
+def sample_rows(w: Workload, n: int, seed: int = 1234):
+    """Seeded (token, q head) samples over valid rows: first/last rows of each
+    sequence plus uniform draws."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for b, c in enumerate(w.chunk_lens):
+        if c == 0:
+            continue
+        for i in sorted({0, c - 1, min(c - 1, 127), min(c - 1, 128)}):
+            out.append((b * w.chunk + i, int(rng.integers(w.num_q_heads))))
+    valid = [(b, c) for b, c in enumerate(w.chunk_lens) if c > 0]
+    while len(out) < n:
+        b, c = valid[int(rng.integers(len(valid)))]
+        out.append((b * w.chunk + int(rng.integers(c)), int(rng.integers(w.num_q_heads))))
+    return out
