@@ -1,0 +1,161 @@
+/*
+ * cpattn -- chunked-prefill GQA attention for GB300 (sm_103a), C ABI.
+ *
+ * One prefill step of a long-context request: a new chunk of queries attends
+ * to (a) its sequence's already-cached KV prefix, fully visible, and (b) its
+ * own chunk's KV under a causal mask -- both walked by ONE kernel with ONE
+ * shared online softmax, with no second launch and no log-sum-exp merge
+ * (TPU PR "PCP: in-kernel ring cache phase, fused with the current phase",
+ * Summary and Design sections).  The PR's ring of cache shards over chips
+ * becomes, on one GPU, only the iteration order over a striped cache layout.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - bf16 tensors are raw device pointers to row-major, densely packed data;
+ *    every device base pointer must be 16-byte aligned.
+ *  - "token order" arrays hold B*C rows: sequence b's chunk occupies rows
+ *    [b*C, b*C + C); its first c_b rows are valid, the rest are padding.
+ *  - Striped cache layout [B, NKV, P, S, HD]: token t of sequence b, kv head
+ *    g lives in shard t mod P at row t div P (stripe width one token; the
+ *    PR's "striped" shards and "strided" cache write, Design and Testing
+ *    sections).  Shard s holds n_s(L) = #{t < L : t mod P = s} filled rows.
+ *  - GQA: query head h reads kv head h / (NQ/NKV).
+ *  - Memory the kernels may touch but must ignore (cache rows beyond the
+ *    filled ones, padding rows) must hold FINITE values; non-finite values
+ *    there are undefined behaviour.
+ *  - Host arrays (cache_lens, chunk_lens) are read during the call only.
+ *  - The caller owns every buffer.  Calls are asynchronous on `stream` (a
+ *    cudaStream_t passed as void*); the library never synchronises except in
+ *    cpattn_sync_status, or after each launch when the environment variable
+ *    CPATTN_DEBUG=1 is set.
+ *  - All argument checks run on the host before any launch; a failed check
+ *    launches nothing.  No C++ exception crosses this interface.
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CPATTN_OK = 0,
+  CPATTN_E_INVALID = 1,      /* bad argument: NULL, misaligned, out-of-range size */
+  CPATTN_E_UNSUPPORTED = 2,  /* valid but outside what this build handles */
+  CPATTN_E_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+  CPATTN_E_NOMEM = 4,        /* host or device allocation failed (create only) */
+  CPATTN_E_TIMEOUT = 5       /* a device-side bounded wait expired; context still usable */
+} cpattn_status;
+
+typedef struct {
+  int32_t num_q_heads;     /* NQ >= 1 */
+  int32_t num_kv_heads;    /* NKV >= 1, NQ % NKV == 0 */
+  int32_t head_dim;        /* HD: 128 or 256 */
+  int32_t num_shards;      /* P >= 1 */
+  int32_t shard_capacity;  /* S >= 1 rows per shard per (sequence, kv head) */
+  int32_t chunk_size;      /* C >= 1 padded rows per sequence */
+  float softmax_scale;     /* <= 0 selects 1/sqrt(HD) */
+} cpattn_config;
+
+typedef struct cpattn_ctx cpattn_ctx; /* opaque */
+
+/* Limits of this build (checked on the host). */
+#define CPATTN_MAX_SEQS 128
+#define CPATTN_MAX_ROW_BLOCKS 2048  /* sum over sequences of ceil(c_b / 128) */
+
+/*
+ * Create a context for one attention layer shape.
+ * cfg: host pointer, read during the call.  *out receives the context.
+ * Allocates a few bytes of device memory for the timeout status word on the
+ * current device (skipped, without error, when no device is present; launches
+ * then fail with CPATTN_E_CUDA).
+ * Errors: E_INVALID (NULL, NQ % NKV != 0, sizes < 1), E_UNSUPPORTED (HD not
+ * 128/256), E_NOMEM.
+ */
+cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out);
+
+/*
+ * Strided KV-cache write (the PR's Testing section: the write that must be
+ * bit-exact).  For every sequence b, valid chunk row i < c_b (token position
+ * t = L_b + i) and kv head g:
+ *   k_cache[b, g, t mod P, t div P, :] = k_new[b*C + i, g, :]   (same for V)
+ * A pure bit copy.  Pad rows are not written; no other cache row is touched.
+ *   num_seqs            B, 1..CPATTN_MAX_SEQS
+ *   cache_lens[B]       host int32, L_b >= 0
+ *   chunk_lens[B]       host int32, 0 <= c_b <= C, and L_b + c_b <= P*S
+ *   k_new, v_new        device bf16 [B*C, NKV, HD], token order
+ *   k_cache, v_cache    device bf16 [B, NKV, P, S, HD], written in place
+ * Errors: E_INVALID, E_CUDA.
+ */
+cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
+                              const int32_t* chunk_lens, const void* k_new, const void* v_new,
+                              void* k_cache, void* v_cache, void* stream);
+
+/*
+ * Fused chunked prefill (the PR's Summary and Design sections): for every
+ * sequence b, query head h, valid row i < c_b,
+ *   O[b*C+i, h, :] = softmax_k( scale * <q_i, k_k> ) . v_k
+ * over keys k = {cache tokens 0..L_b-1} U {chunk tokens 0..i} of kv head
+ * h/(NQ/NKV), as one softmax (bf16 inputs, fp32 accumulation, bf16 output).
+ * Cache tokens are read from rows [0, n_s(L_b)) of each shard; the chunk's
+ * own K/V come from k_new/v_new in token order.  write_kv for the same chunk
+ * may run before or after this call.
+ *   q                   device bf16 [B*C, NQ, HD], token order
+ *   k_new, v_new        device bf16 [B*C, NKV, HD]
+ *   k_cache, v_cache    device bf16 [B, NKV, P, S, HD]
+ *   out                 device bf16 [B*C, NQ, HD]; pad rows are not written
+ *   lse                 device fp32 [B*C, NQ] natural-log sum-exp of the
+ *                       scaled logits, or NULL; pad rows not written
+ * Errors: E_INVALID, E_UNSUPPORTED (more than CPATTN_MAX_ROW_BLOCKS row
+ * blocks), E_CUDA.  A device-side timeout is reported by cpattn_sync_status.
+ */
+cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
+                             const int32_t* chunk_lens, const void* q, const void* k_new,
+                             const void* v_new, const void* k_cache, const void* v_cache,
+                             void* out, float* lse, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the context's device status word.
+ * Returns E_TIMEOUT if a kernel launched with this context gave up on a
+ * bounded wait since the last call (its outputs are then incomplete), E_CUDA
+ * on a CUDA error, else OK.
+ */
+cpattn_status cpattn_sync_status(cpattn_ctx* ctx, void* stream);
+
+/*
+ * Testing hook for the bounded-wait failure path.  flags = 1 makes one thread
+ * of the first CTA of later cpattn_prefill launches skip one internal
+ * arrival, so that CTA's waits expire after timeout_ms and it returns early;
+ * cpattn_sync_status then reports E_TIMEOUT.  flags = 0 restores normal
+ * operation.  timeout_ms <= 0 restores the default limit of 1000 ms per wait.
+ */
+cpattn_status cpattn_set_fault_injection(cpattn_ctx* ctx, int32_t flags, int32_t timeout_ms);
+
+/*
+ * Host-side view of the cache walk (no device work): for cache length L and
+ * the context's P and S, writes the flat tile indices the prefill kernel
+ * visits, in order, to tiles[0..n) and each tile's 128-column validity mask
+ * as four 32-bit words to masks[4*i..4*i+4) (bit c of word c/32 set iff flat
+ * row tile*128 + c of the (sequence, kv head) is a filled cache row).  *count
+ * receives n; at most max_tiles entries are written (E_INVALID if more are
+ * needed).  Either output pointer may be NULL to query the count only.
+ */
+cpattn_status cpattn_cache_walk(const cpattn_ctx* ctx, int32_t cache_len, int32_t* tiles,
+                                uint32_t* masks, int32_t max_tiles, int32_t* count);
+
+/* Free the context (NULL-safe).  Does not synchronise. */
+void cpattn_destroy(cpattn_ctx* ctx);
+
+/* Static description of a status code. */
+const char* cpattn_status_string(cpattn_status s);
+
+/* Detail of the last error on this context (empty string if none). */
+const char* cpattn_last_error(const cpattn_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H_ */

@@ -1,0 +1,194 @@
+"""ctypes binding of ``libcpattn.so`` (declared in include/cpattn.h).
+
+Argument marshalling only: every step of the hot path runs in the CUDA
+kernels of the library.  There is no fallback -- if the library is missing
+or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcpattn.so")
+
+OK, E_INVALID, E_UNSUPPORTED, E_CUDA, E_NOMEM, E_TIMEOUT = range(6)
+MAX_SEQS = 128
+MAX_ROW_BLOCKS = 2048
+
+# Every symbol include/cpattn.h declares.
+EXPORTS = ("cpattn_create", "cpattn_write_kv", "cpattn_prefill", "cpattn_sync_status",
+           "cpattn_set_fault_injection", "cpattn_cache_walk", "cpattn_destroy",
+           "cpattn_status_string", "cpattn_last_error")
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"cpattn status {status}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("num_shards", ctypes.c_int32),
+                ("shard_capacity", ctypes.c_int32), ("chunk_size", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing: build it with "
+                           "long_context_chunked_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, U32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32
+    I32P = ctypes.POINTER(ctypes.c_int32)
+    lib.cpattn_create.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(P)]
+    lib.cpattn_create.restype = I32
+    lib.cpattn_write_kv.argtypes = [P, I32, I32P, I32P, P, P, P, P, P]
+    lib.cpattn_write_kv.restype = I32
+    lib.cpattn_prefill.argtypes = [P, I32, I32P, I32P, P, P, P, P, P, P, P, P]
+    lib.cpattn_prefill.restype = I32
+    lib.cpattn_sync_status.argtypes = [P, P]
+    lib.cpattn_sync_status.restype = I32
+    lib.cpattn_set_fault_injection.argtypes = [P, I32, I32]
+    lib.cpattn_set_fault_injection.restype = I32
+    lib.cpattn_cache_walk.argtypes = [P, I32, I32P, ctypes.POINTER(U32), I32, I32P]
+    lib.cpattn_cache_walk.restype = I32
+    lib.cpattn_destroy.argtypes = [P]
+    lib.cpattn_destroy.restype = None
+    lib.cpattn_status_string.argtypes = [I32]
+    lib.cpattn_status_string.restype = ctypes.c_char_p
+    lib.cpattn_last_error.argtypes = [P]
+    lib.cpattn_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _i32(values: Sequence[int]):
+    arr = np.ascontiguousarray(np.asarray(values, dtype=np.int32))
+    return arr, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _ptr(t) -> int:
+    """Device pointer of a tensor, or an int passed through; None -> NULL."""
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Context:
+    """One attention-layer shape: NQ, NKV, HD, shard count P, shard capacity S, chunk C."""
+
+    def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, num_shards: int,
+                 shard_capacity: int, chunk_size: int, softmax_scale: float = 0.0):
+        self.lib = load()
+        self.cfg = Config(num_q_heads, num_kv_heads, head_dim, num_shards, shard_capacity,
+                          chunk_size, softmax_scale)
+        h = ctypes.c_void_p()
+        st = self.lib.cpattn_create(ctypes.byref(self.cfg), ctypes.byref(h))
+        if st != OK:
+            raise CpattnError(st, self.lib.cpattn_status_string(st).decode())
+        self._h = h
+
+    @classmethod
+    def for_workload(cls, w) -> "Context":
+        return cls(w.num_q_heads, w.num_kv_heads, w.head_dim, w.shards, w.shard_capacity,
+                   w.chunk, w.scale)
+
+    # -- status --------------------------------------------------------
+    def _check(self, st: int):
+        if st != OK:
+            msg = self.lib.cpattn_last_error(self._h).decode() or \
+                self.lib.cpattn_status_string(st).decode()
+            raise CpattnError(st, msg)
+
+    def status(self, st: int) -> int:
+        return st
+
+    # -- entry points --------------------------------------------------
+    def write_kv_raw(self, cache_lens, chunk_lens, k_new, v_new, k_cache, v_cache, stream=None) -> int:
+        cl, clp = _i32(cache_lens)
+        ch, chp = _i32(chunk_lens)
+        return self.lib.cpattn_write_kv(self._h, len(cl), clp, chp, _ptr(k_new), _ptr(v_new),
+                                        _ptr(k_cache), _ptr(v_cache), _stream(stream))
+
+    def write_kv(self, cache_lens, chunk_lens, k_new, v_new, k_cache, v_cache, stream=None):
+        self._check_tensors((k_new, v_new, k_cache, v_cache))
+        self._check(self.write_kv_raw(cache_lens, chunk_lens, k_new, v_new, k_cache, v_cache,
+                                      stream))
+
+    def prefill_raw(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out,
+                    lse=None, stream=None) -> int:
+        cl, clp = _i32(cache_lens)
+        ch, chp = _i32(chunk_lens)
+        return self.lib.cpattn_prefill(self._h, len(cl), clp, chp, _ptr(q), _ptr(k_new),
+                                       _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                       _ptr(lse), _stream(stream))
+
+    def prefill(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out, lse=None,
+                stream=None):
+        self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
+        self._check(self.prefill_raw(cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
+                                     out, lse, stream))
+
+    def sync_status(self, stream=None) -> int:
+        """Synchronise and return the status code (E_TIMEOUT if a device wait expired)."""
+        return self.lib.cpattn_sync_status(self._h, _stream(stream))
+
+    def set_fault_injection(self, flags: int, timeout_ms: int = 0):
+        self._check(self.lib.cpattn_set_fault_injection(self._h, flags, timeout_ms))
+
+    def cache_walk(self, cache_len: int):
+        """(tiles int32 [n], masks uint32 [n, 4]) of the kernel's cache walk."""
+        n = ctypes.c_int32()
+        self._check(self.lib.cpattn_cache_walk(self._h, cache_len, None, None, 0, ctypes.byref(n)))
+        tiles = np.zeros(max(n.value, 1), dtype=np.int32)
+        masks = np.zeros((max(n.value, 1), 4), dtype=np.uint32)
+        self._check(self.lib.cpattn_cache_walk(
+            self._h, cache_len, tiles.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            masks.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), n.value, ctypes.byref(n)))
+        return tiles[:n.value], masks[:n.value]
+
+    def last_error(self) -> str:
+        return self.lib.cpattn_last_error(self._h).decode()
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self.lib.cpattn_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _check_tensors(ts):
+        import torch
+        for t in ts:
+            if t is None or isinstance(t, int):
+                continue
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("expected contiguous bf16 CUDA tensors")

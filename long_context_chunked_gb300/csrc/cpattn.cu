@@ -1,0 +1,340 @@
+// C-ABI library: argument checks, tensor-map encoding, launches.
+// Declarations and contracts: include/cpattn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "cpattn.h"
+#include "prefill.cuh"
+#include "walk.cuh"
+#include "write_kv.cuh"
+
+struct cpattn_ctx {
+  cpattn_config cfg;
+  int device = -1;
+  int num_sms = 0;
+  int* d_status = nullptr;           // device status word (timeouts)
+  bool attr_set_128 = false, attr_set_256 = false;
+  int debug_flags = 0;
+  unsigned long long timeout_ns = 1000ull * 1000 * 1000;
+  bool debug_sync = false;
+  std::string last_error;
+};
+
+namespace {
+
+using cpattn::kBKV;
+using cpattn::kBQ;
+
+cpattn_status fail(cpattn_ctx* ctx, cpattn_status s, const std::string& msg) {
+  if (ctx != nullptr) ctx->last_error = msg;
+  return s;
+}
+
+cpattn_status cuda_fail(cpattn_ctx* ctx, cudaError_t e, const char* what) {
+  return fail(ctx, CPATTN_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map with 128-byte swizzle: dims (d0 innermost), byte
+// strides of dims 1 and 2, box (b0, b1, b2).
+bool encode3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t st1, uint64_t st2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {st1, st2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Checks shared by write_kv and prefill.
+cpattn_status check_seqs(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
+                         const int32_t* chunk_lens) {
+  if (num_seqs < 1) return fail(ctx, CPATTN_E_INVALID, "num_seqs must be >= 1");
+  if (num_seqs > CPATTN_MAX_SEQS)
+    return fail(ctx, CPATTN_E_UNSUPPORTED,
+                "num_seqs " + std::to_string(num_seqs) + " exceeds CPATTN_MAX_SEQS");
+  if (cache_lens == nullptr || chunk_lens == nullptr)
+    return fail(ctx, CPATTN_E_INVALID, "cache_lens / chunk_lens must not be NULL");
+  const cpattn_config& c = ctx->cfg;
+  const long long cap = static_cast<long long>(c.num_shards) * c.shard_capacity;
+  for (int b = 0; b < num_seqs; ++b) {
+    if (cache_lens[b] < 0)
+      return fail(ctx, CPATTN_E_INVALID, "cache_lens[" + std::to_string(b) + "] < 0");
+    if (chunk_lens[b] < 0 || chunk_lens[b] > c.chunk_size)
+      return fail(ctx, CPATTN_E_INVALID,
+                  "chunk_lens[" + std::to_string(b) + "] outside [0, chunk_size]");
+    if (static_cast<long long>(cache_lens[b]) + chunk_lens[b] > cap)
+      return fail(ctx, CPATTN_E_INVALID,
+                  "sequence " + std::to_string(b) + ": cache_len + chunk_len exceeds P*S");
+  }
+  const long long cache_rows =
+      static_cast<long long>(num_seqs) * c.num_kv_heads * c.num_shards * c.shard_capacity;
+  const long long tokens = static_cast<long long>(num_seqs) * c.chunk_size;
+  if (cache_rows + kBKV >= (1LL << 31) || tokens + kBQ >= (1LL << 31))
+    return fail(ctx, CPATTN_E_UNSUPPORTED, "cache or token row count exceeds 2^31");
+  return CPATTN_OK;
+}
+
+cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, what);
+  if (ctx->debug_sync) return cpattn_sync_status(ctx, stream);
+  return CPATTN_OK;
+}
+
+template <int HD>
+cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
+  using Ly = cpattn::Layout<HD>;
+  bool& attr = HD == 256 ? ctx->attr_set_256 : ctx->attr_set_128;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(cpattn::prefill_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Ly::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(prefill)");
+    attr = true;
+  }
+  const int grid = std::min(prm->num_units, ctx->num_sms);
+  cpattn::prefill_kernel<HD><<<grid, 192, Ly::SMEM_BYTES, stream>>>(*prm);
+  return after_launch(ctx, stream, "prefill launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cpattn_status_string(cpattn_status s) {
+  switch (s) {
+    case CPATTN_OK: return "ok";
+    case CPATTN_E_INVALID: return "invalid argument";
+    case CPATTN_E_UNSUPPORTED: return "unsupported by this build";
+    case CPATTN_E_CUDA: return "CUDA error";
+    case CPATTN_E_NOMEM: return "out of memory";
+    case CPATTN_E_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* cpattn_last_error(const cpattn_ctx* ctx) {
+  return ctx == nullptr ? "" : ctx->last_error.c_str();
+}
+
+cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
+  if (out == nullptr || cfg == nullptr) return CPATTN_E_INVALID;
+  *out = nullptr;
+  const cpattn_config& c = *cfg;
+  if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
+      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0)
+    return CPATTN_E_INVALID;
+  if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
+  if (c.num_q_heads > 65535) return CPATTN_E_UNSUPPORTED;
+  cpattn_ctx* ctx = new (std::nothrow) cpattn_ctx();
+  if (ctx == nullptr) return CPATTN_E_NOMEM;
+  ctx->cfg = c;
+  if (!(c.softmax_scale > 0.f)) ctx->cfg.softmax_scale = 1.0f / std::sqrt(static_cast<float>(c.head_dim));
+  const char* dbg = std::getenv("CPATTN_DEBUG");
+  ctx->debug_sync = dbg != nullptr && dbg[0] == '1';
+  int dev = -1, ndev = 0;
+  if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0 && cudaGetDevice(&dev) == cudaSuccess) {
+    ctx->device = dev;
+    cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaMalloc(&ctx->d_status, sizeof(int)) != cudaSuccess ||
+        cudaMemset(ctx->d_status, 0, sizeof(int)) != cudaSuccess) {
+      cudaFree(ctx->d_status);
+      delete ctx;
+      return CPATTN_E_NOMEM;
+    }
+  } else {
+    cudaGetLastError();  // clear the "no device" error
+  }
+  *out = ctx;
+  return CPATTN_OK;
+}
+
+void cpattn_destroy(cpattn_ctx* ctx) {
+  if (ctx == nullptr) return;
+  if (ctx->d_status != nullptr) cudaFree(ctx->d_status);
+  delete ctx;
+}
+
+cpattn_status cpattn_set_fault_injection(cpattn_ctx* ctx, int32_t flags, int32_t timeout_ms) {
+  if (ctx == nullptr || flags < 0 || flags > 1) return CPATTN_E_INVALID;
+  ctx->debug_flags = flags;
+  ctx->timeout_ns = timeout_ms > 0 ? static_cast<unsigned long long>(timeout_ms) * 1000000ull
+                                   : 1000ull * 1000 * 1000;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_cache_walk(const cpattn_ctx* ctx, int32_t cache_len, int32_t* tiles,
+                                uint32_t* masks, int32_t max_tiles, int32_t* count) {
+  if (ctx == nullptr || count == nullptr || cache_len < 0 || max_tiles < 0) return CPATTN_E_INVALID;
+  const int P = ctx->cfg.num_shards, S = ctx->cfg.shard_capacity;
+  if (static_cast<long long>(cache_len) > static_cast<long long>(P) * S) return CPATTN_E_INVALID;
+  cpattn::CacheWalk w;
+  w.init(cache_len, P, S);
+  int n = 0;
+  while (!w.done()) {
+    const int t = w.next();
+    if ((tiles != nullptr || masks != nullptr) && n >= max_tiles) return CPATTN_E_INVALID;
+    if (tiles != nullptr) tiles[n] = t;
+    if (masks != nullptr) {
+      uint32_t mw[4];
+      w.column_mask(t, mw);
+      std::memcpy(masks + 4 * n, mw, sizeof(mw));
+    }
+    ++n;
+  }
+  *count = n;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_sync_status(cpattn_ctx* ctx, void* stream) {
+  if (ctx == nullptr) return CPATTN_E_INVALID;
+  if (ctx->d_status == nullptr) return fail(ctx, CPATTN_E_CUDA, "no CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpy(&word, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "reading the status word");
+  if (word != 0) {
+    cudaMemset(ctx->d_status, 0, sizeof(int));
+    return fail(ctx, CPATTN_E_TIMEOUT,
+                "a bounded device wait expired (site " + std::to_string(word >> 8) + ")");
+  }
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
+                              const int32_t* chunk_lens, const void* k_new, const void* v_new,
+                              void* k_cache, void* v_cache, void* stream) {
+  if (ctx == nullptr) return CPATTN_E_INVALID;
+  cpattn_status s = check_seqs(ctx, num_seqs, cache_lens, chunk_lens);
+  if (s != CPATTN_OK) return s;
+  if (k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr)
+    return fail(ctx, CPATTN_E_INVALID, "device pointers must not be NULL");
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(ctx, CPATTN_E_INVALID, "device pointers must be 16-byte aligned");
+  const cpattn_config& c = ctx->cfg;
+  cpattn::WriteKvParams p;
+  p.k_new = static_cast<const uint4*>(k_new);
+  p.v_new = static_cast<const uint4*>(v_new);
+  p.k_cache = static_cast<uint4*>(k_cache);
+  p.v_cache = static_cast<uint4*>(v_cache);
+  p.num_seqs = num_seqs;
+  p.nkv = c.num_kv_heads;
+  p.P = c.num_shards;
+  p.S = c.shard_capacity;
+  p.C = c.chunk_size;
+  p.vec_per_row = c.head_dim * 2 / 16;
+  long long acc = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    p.cache_len[b] = cache_lens[b];
+    p.vec_prefix[b] = acc;
+    acc += static_cast<long long>(chunk_lens[b]) * c.num_kv_heads * p.vec_per_row;
+  }
+  p.vec_prefix[num_seqs] = acc;
+  p.total_vecs = acc;
+  if (acc == 0) return CPATTN_OK;
+  if (ctx->d_status == nullptr) return fail(ctx, CPATTN_E_CUDA, "no CUDA device");
+  const long long blocks = (acc + 255) / 256;
+  const int grid = static_cast<int>(std::min<long long>(blocks, static_cast<long long>(ctx->num_sms) * 16));
+  cpattn::write_kv_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  return after_launch(ctx, static_cast<cudaStream_t>(stream), "write_kv launch");
+}
+
+cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
+                             const int32_t* chunk_lens, const void* q, const void* k_new,
+                             const void* v_new, const void* k_cache, const void* v_cache,
+                             void* out, float* lse, void* stream) {
+  if (ctx == nullptr) return CPATTN_E_INVALID;
+  cpattn_status s = check_seqs(ctx, num_seqs, cache_lens, chunk_lens);
+  if (s != CPATTN_OK) return s;
+  if (q == nullptr || k_new == nullptr || v_new == nullptr || k_cache == nullptr ||
+      v_cache == nullptr || out == nullptr)
+    return fail(ctx, CPATTN_E_INVALID, "device pointers must not be NULL");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)))
+    return fail(ctx, CPATTN_E_INVALID, "device pointers must be 16-byte aligned");
+  const cpattn_config& c = ctx->cfg;
+
+  // Row blocks (b, q block), longest first: a unit's cost is its tile count.
+  struct Blk { int work, b, qb; };
+  std::vector<Blk> blks;
+  std::vector<int> ncache(num_seqs);
+  for (int b = 0; b < num_seqs; ++b) {
+    ncache[b] = cpattn::cache_tile_count(cache_lens[b], c.num_shards, c.shard_capacity);
+    const int nqb = (chunk_lens[b] + kBQ - 1) / kBQ;
+    for (int qb = 0; qb < nqb; ++qb) blks.push_back({ncache[b] + qb + 1, b, qb});
+  }
+  if (blks.size() > CPATTN_MAX_ROW_BLOCKS)
+    return fail(ctx, CPATTN_E_UNSUPPORTED, "more than CPATTN_MAX_ROW_BLOCKS row blocks");
+  if (blks.empty()) return CPATTN_OK;
+  if (ctx->d_status == nullptr) return fail(ctx, CPATTN_E_CUDA, "no CUDA device");
+  std::stable_sort(blks.begin(), blks.end(), [](const Blk& a, const Blk& b) { return a.work > b.work; });
+
+  static thread_local cpattn::PrefillParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
+  const uint64_t T = static_cast<uint64_t>(num_seqs) * c.chunk_size;
+  const uint64_t rows = static_cast<uint64_t>(num_seqs) * NKV * c.num_shards * c.shard_capacity;
+  const uint32_t vrows = 8192u / static_cast<uint32_t>(HD);
+  const uint64_t rb = static_cast<uint64_t>(HD) * 2;
+  bool ok = encode3d(&prm.tm_q, q, HD, NQ, T, rb, rb * NQ, 64, 1, kBQ) &&
+            encode3d(&prm.tm_k_new, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV) &&
+            encode3d(&prm.tm_v_new, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, vrows) &&
+            encode3d(&prm.tm_k_cache, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV) &&
+            encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows);
+  if (!ok) return fail(ctx, CPATTN_E_CUDA, "cuTensorMapEncodeTiled failed");
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.status = ctx->d_status;
+  prm.timeout_ns = ctx->timeout_ns;
+  prm.nq = NQ;
+  prm.nkv = NKV;
+  prm.group = NQ / NKV;
+  prm.P = c.num_shards;
+  prm.S = c.shard_capacity;
+  prm.C = c.chunk_size;
+  prm.debug_flags = ctx->debug_flags;
+  prm.scale_log2 = c.softmax_scale * 1.4426950408889634f;
+  for (int b = 0; b < num_seqs; ++b)
+    prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], ncache[b], 0};
+  for (size_t i = 0; i < blks.size(); ++i)
+    prm.blocks[i] = (static_cast<uint32_t>(blks[i].b) << 16) | static_cast<uint32_t>(blks[i].qb);
+  prm.num_units = static_cast<int>(blks.size()) * NQ;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return HD == 256 ? launch_prefill<256>(ctx, &prm, st) : launch_prefill<128>(ctx, &prm, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,503 @@
+// Fused chunked-prefill attention for sm_103a: cache region and current
+// region walked by ONE kernel with ONE online softmax (PCP ring-cache PR,
+// Summary and Design sections), on the 5th-generation tensor cores.
+//
+// Work unit: (sequence b, query head h, q block of 128 rows).  A persistent
+// grid of one CTA per SM walks units longest first.  Per unit the CTA runs a
+// virtual tile index v over n_cache cache tiles (the striped-shard walk of
+// walk.cuh) followed by the causal current tiles 0..qb; the region of tile v
+// is selected by the value of one scalar (in_cache = v < n_cache): it picks
+// the tensor map and coordinates of the tile loads and the column mask.
+//
+// Roles (192 threads):
+//   warps 0-3  softmax: tcgen05.ld S row-per-thread, value mask, online
+//              (m, l) update with lazy O rescale, P (bf16) back into TMEM
+//              over S's columns, epilogue O / l -> bf16 global stores.
+//   warp 4     TMA producer: Q once per unit, then K/V sub-tiles into a ring
+//              of 16 KB shared-memory slots.
+//   warp 5     TMEM allocation and the single MMA-issuing thread:
+//              S = Q K^T (both operands in shared memory) and
+//              O += P V (P from TMEM, V from shared memory).
+//
+// TMEM (512 columns x 128 lanes, fp32): O at [0, HD), S double buffer at
+// [HD, HD+128) and [HD+128, HD+256).  P_t is written over the first 64
+// columns of its S buffer; MMAs of one thread execute in issue order, so the
+// QK^T that next overwrites that buffer (tile t+2) runs after PV_t read P_t.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "walk.cuh"
+
+namespace cpattn {
+
+struct SeqInfo {
+  int cache_len, chunk_len, n_cache_tiles, pad;
+};
+
+struct PrefillParams {
+  CUtensorMap tm_q;        // [T, NQ, HD]       box 64 x 1 x 128
+  CUtensorMap tm_k_new;    // [T, NKV, HD]      box 64 x 1 x 128
+  CUtensorMap tm_v_new;    // [T, NKV, HD]      box 64 x 1 x VROWS
+  CUtensorMap tm_k_cache;  // [rows, 1, HD]     box 64 x 1 x 128
+  CUtensorMap tm_v_cache;  // [rows, 1, HD]     box 64 x 1 x VROWS
+  __nv_bfloat16* out;
+  float* lse;
+  int* status;
+  unsigned long long timeout_ns;
+  int num_units, nq, nkv, group, P, S, C, debug_flags;
+  float scale_log2;
+  SeqInfo seqs[CPATTN_MAX_SEQS];
+  uint32_t blocks[CPATTN_MAX_ROW_BLOCKS];  // (b << 16) | q block, longest first
+};
+
+enum : int { kDebugDropArrive = 1 };
+
+// Sites recorded in the status word when a bounded wait expires.
+enum : int {
+  kSiteQEmpty = 1, kSiteSlotEmpty, kSiteQFull, kSiteSlotFull, kSitePFull, kSiteSFull,
+  kSiteODone, kSiteDrain
+};
+
+template <int HD>
+struct Layout {
+  static constexpr int KCH = HD / 64;            // 64-column chunks per row (one TMA box each)
+  static constexpr int VROWS = 8192 / HD;        // kv rows per V sub-tile (16 KB)
+  static constexpr int VSUB = kBKV / VROWS;      // V sub-tiles per tile
+  static constexpr int SUB = 16384;              // bytes per ring slot
+  static constexpr int Q_BYTES = kBQ * HD * 2;
+  static constexpr int NSLOT = HD == 256 ? 10 : 12;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * SUB;
+  // barrier indices
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_SFULL = 2, B_PFULL = 4, B_ODONE = 6,
+                       B_DRAIN = 7, B_SLOTFULL = 8, B_SLOTEMPTY = 8 + NSLOT;
+  static constexpr int NBAR = 8 + 2 * NSLOT;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_QK = make_idesc_bf16(kBQ, kBKV, false);
+  static constexpr uint32_t IDESC_PV = make_idesc_bf16(kBQ, HD, true);
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(HD + 2 * kBKV <= TMEM_COLS, "TMEM budget");
+};
+
+struct Unit {
+  int b, h, g, qb, q0, L, c, n_cache, n_tiles;
+};
+
+__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
+  Unit U;
+  const int blk = u / p.nq;
+  U.h = u - blk * p.nq;
+  const uint32_t e = p.blocks[blk];
+  U.b = static_cast<int>(e >> 16);
+  U.qb = static_cast<int>(e & 0xFFFFu);
+  U.g = U.h / p.group;
+  U.q0 = U.qb * kBQ;
+  U.L = p.seqs[U.b].cache_len;
+  U.c = p.seqs[U.b].chunk_len;
+  U.n_cache = p.seqs[U.b].n_cache_tiles;
+  U.n_tiles = U.n_cache + U.qb + 1;
+  return U;
+}
+
+// Ring position shared by producer and consumer.
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;  // parity of the current use of `slot`
+  uint32_t round = 0;  // 0 during the first pass over the ring
+  template <int NSLOT>
+  __device__ __forceinline__ void advance() {
+    if (++slot == NSLOT) {
+      slot = 0;
+      phase ^= 1u;
+      round = 1;
+    }
+  }
+};
+
+}  // namespace cpattn
+
+namespace cpattn {
+
+constexpr unsigned long long kDrainLimitNs = 200ull * 1000 * 1000;
+
+// ------------------------------------------------------------- TMA producer
+template <int HD>
+__device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t sbase,
+                                              const BoundedWait& wait) {
+  using Ly = Layout<HD>;
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  RingPos rp;
+  long long issued = 0;
+  uint32_t q_issued = 0;
+  bool ok = true;
+
+  // One 16 KB ring slot: wait until the MMA released it, then `nbox` boxes
+  // of 64 columns starting at column x0.
+  auto load_sub = [&](const CUtensorMap* m, int x0, int y, int z, int nbox, int box_bytes) {
+    if (rp.round && !wait(bar(Ly::B_SLOTEMPTY + rp.slot), rp.phase ^ 1u, kSiteSlotEmpty))
+      return false;
+    const uint32_t full = bar(Ly::B_SLOTFULL + rp.slot);
+    mbar_arrive_expect_tx(full, Ly::SUB);
+    const uint32_t dst = sbase + Ly::OFF_RING + static_cast<uint32_t>(rp.slot) * Ly::SUB;
+    for (int i = 0; i < nbox; ++i) tma_load_3d(dst + i * box_bytes, m, full, x0 + 64 * i, y, z);
+    rp.template advance<Ly::NSLOT>();
+    ++issued;
+    return true;
+  };
+
+  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+    const Unit U = decode_unit(p, u);
+    if (q_issued > 0 && !wait(bar(Ly::B_QEMPTY), (q_issued - 1) & 1u, kSiteQEmpty)) {
+      ok = false;
+      break;
+    }
+    mbar_arrive_expect_tx(bar(Ly::B_QFULL), Ly::Q_BYTES);
+    for (int c = 0; c < Ly::KCH; ++c)
+      tma_load_3d(sbase + Ly::OFF_Q + c * (kBQ * 128), &p.tm_q, bar(Ly::B_QFULL), 64 * c, U.h,
+                  U.b * p.C + U.q0);
+    ++q_issued;
+
+    const int head_row = ((U.b * p.nkv + U.g) * p.P) * p.S;
+    CacheWalk wk, wv;
+    wk.init(U.L, p.P, p.S);
+    wv.init(U.L, p.P, p.S);
+    // Tile v's source is chosen by value: cache map and shard-walk row, or
+    // the chunk's token-order map and row.
+    auto load_k = [&](int v) {
+      const bool in_cache = v < U.n_cache;
+      const int tile = in_cache ? wk.next() : 0;
+      const CUtensorMap* m = in_cache ? &p.tm_k_cache : &p.tm_k_new;
+      const int y = in_cache ? 0 : U.g;
+      const int z = in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV;
+      for (int c = 0; c < Ly::KCH; ++c)
+        if (!load_sub(m, 64 * c, y, z, 1, 0)) return false;
+      return true;
+    };
+    auto load_v = [&](int v) {
+      const bool in_cache = v < U.n_cache;
+      const int tile = in_cache ? wv.next() : 0;
+      const CUtensorMap* m = in_cache ? &p.tm_v_cache : &p.tm_v_new;
+      const int y = in_cache ? 0 : U.g;
+      const int z = in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV;
+      for (int j = 0; j < Ly::VSUB; ++j)
+        if (!load_sub(m, 0, y, z + j * Ly::VROWS, Ly::KCH, Ly::VROWS * 128)) return false;
+      return true;
+    };
+    // Same order as the MMA consumes them: K0, (K1, V0), (K2, V1), ..., V_last.
+    ok = load_k(0);
+    for (int v = 1; ok && v < U.n_tiles; ++v) ok = load_k(v) && load_v(v - 1);
+    if (ok) ok = load_v(U.n_tiles - 1);
+  }
+
+  if (!ok) {
+    // Let copies already issued land before this CTA can exit.
+    const long long first = issued > Ly::NSLOT ? issued - Ly::NSLOT : 0;
+    for (long long z = first; z < issued; ++z)
+      mbar_wait_drain(bar(Ly::B_SLOTFULL + static_cast<int>(z % Ly::NSLOT)),
+                      static_cast<uint32_t>((z / Ly::NSLOT) & 1), kDrainLimitNs);
+    if (q_issued > 0) mbar_wait_drain(bar(Ly::B_QFULL), (q_issued - 1) & 1u, kDrainLimitNs);
+  }
+}
+
+// ------------------------------------------------------------- MMA issuer
+template <int HD>
+__device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
+                                         const BoundedWait& wait) {
+  using Ly = Layout<HD>;
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  const uint32_t q_base = sbase + Ly::OFF_Q;
+  const uint32_t ring = sbase + Ly::OFF_RING;
+  RingPos rp;
+  uint32_t tile_ctr = 0, units = 0;
+  bool ok = true;
+
+  // O (+)= P_w V_w, P_w from the S buffer of global tile t.
+  auto issue_pv = [&](int w, uint32_t t) {
+    const uint32_t sb = t & 1u;
+    if (!wait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
+    tc_fence_after();
+    const uint32_t p_tmem = tmem + HD + sb * kBKV;
+    for (int j = 0; j < Ly::VSUB; ++j) {
+      if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
+      tc_fence_after();
+      const uint32_t vb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
+#pragma unroll
+      for (int kk = 0; kk < Ly::VROWS / 16; ++kk) {
+        // V sub-tile: KCH column chunks of VROWS rows x 128 B, N-contiguous.
+        const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, Ly::VROWS * 128, 1024);
+        mma_ts(tmem, p_tmem + (j * Ly::VROWS + kk * 16) / 2, bd, Ly::IDESC_PV,
+               (w | j | kk) != 0);
+      }
+      mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
+      rp.template advance<Ly::NSLOT>();
+    }
+    mma_commit(bar(Ly::B_ODONE));
+    return true;
+  };
+
+  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
+    const Unit U = decode_unit(p, u);
+    if (!wait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    for (int v = 0; v < U.n_tiles; ++v) {
+      const uint32_t sb = tile_ctr & 1u;
+      const uint32_t s_tmem = tmem + HD + sb * kBKV;
+      for (int c = 0; c < Ly::KCH; ++c) {
+        if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = make_sdesc_sw128(q_base + c * (kBQ * 128) + kk * 32, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(kb + kk * 32, 16, 1024);
+          mma_ss(s_tmem, ad, bd, Ly::IDESC_QK, (c | kk) != 0);
+        }
+        mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
+        rp.template advance<Ly::NSLOT>();
+      }
+      if (!ok) break;
+      mma_commit(bar(Ly::B_SFULL + sb));
+      if (v == U.n_tiles - 1) mma_commit(bar(Ly::B_QEMPTY));
+      if (v >= 1 && !issue_pv(v - 1, tile_ctr - 1)) {
+        ok = false;
+        break;
+      }
+      ++tile_ctr;
+    }
+    if (ok) ok = issue_pv(U.n_tiles - 1, tile_ctr - 1);
+  }
+  // Every MMA issued must complete before TMEM is released.
+  mma_commit(bar(Ly::B_DRAIN));
+  mbar_wait_drain(bar(Ly::B_DRAIN), 0u, kDrainLimitNs);
+}
+}  // namespace cpattn
+
+namespace cpattn {
+
+// Column-validity words of a current-region tile for query row r: on the
+// diagonal tile key column c is visible iff c <= r (causal, diagonal
+// inclusive); tiles left of the diagonal are fully visible.
+__device__ __forceinline__ uint32_t causal_word(int lim, int q) {
+  const int n = lim - 32 * q;
+  return n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+// ------------------------------------------------------- softmax + epilogue
+template <int HD>
+__device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
+                                             const BoundedWait& wait) {
+  using Ly = Layout<HD>;
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  const int r = threadIdx.x;  // query row within the 128-row block == TMEM lane
+  const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(r & ~31) << 16);
+  const float sl2 = p.scale_log2;
+  uint32_t tile_ctr = 0;
+  bool drop_one = (p.debug_flags & kDebugDropArrive) && blockIdx.x == 0 && r == 0;
+
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    const Unit U = decode_unit(p, u);
+    CacheWalk walk;
+    walk.init(U.L, p.P, p.S);
+    float m = -INFINITY;  // running max of the scaled logits, log2 units
+    float l = 0.f;        // running sum of 2^(x - m)
+    bool ok = true;
+
+    for (int v = 0; v < U.n_tiles; ++v) {
+      const uint32_t sb = tile_ctr & 1u;
+      ok = wait(bar(Ly::B_SFULL + sb), (tile_ctr >> 1) & 1u, kSiteSFull);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_tmem = lane_tmem + HD + sb * kBKV;
+      float s[kBKV];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t raw[32];
+        tmem_ld32_wait(s_tmem + 32 * q, raw);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 * q + i] = __uint_as_float(raw[i]);
+      }
+
+      // Region by value: one scalar picks the validity words.
+      const bool in_cache = v < U.n_cache;
+      uint32_t mw[4];
+      if (in_cache) {
+        walk.column_mask(walk.next(), mw);
+      } else {
+        const int lim = (v - U.n_cache == U.qb) ? r + 1 : kBKV;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mw[q] = causal_word(lim, q);
+      }
+      const bool need_mask = __any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < kBKV; ++c)
+          s[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
+      }
+
+      float mt0 = s[0], mt1 = s[1], mt2 = s[2], mt3 = s[3];
+#pragma unroll
+      for (int c = 4; c < kBKV; c += 4) {
+        mt0 = fmaxf(mt0, s[c]);
+        mt1 = fmaxf(mt1, s[c + 1]);
+        mt2 = fmaxf(mt2, s[c + 2]);
+        mt3 = fmaxf(mt3, s[c + 3]);
+      }
+      const float m_tile = fmaxf(fmaxf(mt0, mt1), fmaxf(mt2, mt3)) * sl2;
+      const float m_new = fmaxf(m, m_tile);
+      if (v == 0) {
+        m = m_new;
+      } else {
+        // Lazy rescale: keep the old reference max unless the new one exceeds
+        // it by more than 2^8; the final O / l is the same either way.
+        const bool need = m_new > m + 8.f;
+        if (__any_sync(0xFFFFFFFFu, need)) {
+          const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+          if (need) m = m_new;
+          ok = wait(bar(Ly::B_ODONE), (tile_ctr - 1) & 1u, kSiteODone);  // PV of tile t-1
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32_wait(lane_tmem + 32 * ch, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(lane_tmem + 32 * ch, o);
+          }
+          tmem_wait_st();
+          l *= alpha;
+        }
+      }
+
+      // p = 2^(x - m), row sum, bf16 pack into the first 64 columns of S.
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      float l0 = 0.f, l1 = 0.f;
+      uint32_t pk0[32], pk1[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float a = ex2_approx(fmaf(s[2 * i], sl2, neg_m));
+        const float b = ex2_approx(fmaf(s[2 * i + 1], sl2, neg_m));
+        l0 += a;
+        l1 += b;
+        pk0[i] = pack_bf16x2(a, b);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float a = ex2_approx(fmaf(s[64 + 2 * i], sl2, neg_m));
+        const float b = ex2_approx(fmaf(s[64 + 2 * i + 1], sl2, neg_m));
+        l0 += a;
+        l1 += b;
+        pk1[i] = pack_bf16x2(a, b);
+      }
+      l += l0 + l1;
+      tmem_st32(s_tmem, pk0);
+      tmem_st32(s_tmem + 32, pk1);
+      tmem_wait_st();
+      tc_fence_before();
+      if (drop_one) {
+        drop_one = false;  // fault-injection hook: this arrival never happens
+      } else {
+        mbar_arrive(bar(Ly::B_PFULL + sb));
+      }
+      ++tile_ctr;
+    }
+    if (!ok) break;
+
+    // Epilogue: O / l -> bf16, valid rows only.
+    ok = wait(bar(Ly::B_ODONE), (tile_ctr - 1) & 1u, kSiteODone);
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (!ok) break;
+    tc_fence_after();
+    const int row = U.q0 + r;
+    const bool valid = row < U.c;
+    const float inv_l = 1.f / l;
+    const long long tok = static_cast<long long>(U.b) * p.C + row;
+    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * p.nq + U.h) * HD);
+#pragma unroll 1
+    for (int ch = 0; ch < HD / 32; ++ch) {
+      uint32_t o[32];
+      tmem_ld32_wait(lane_tmem + 32 * ch, o);
+      if (valid) {
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 pk;
+          pk.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
+          pk.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
+          pk.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
+          pk.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
+          orow[ch * 4 + v4] = pk;
+        }
+      }
+    }
+    if (valid && p.lse != nullptr) p.lse[tok * p.nq + U.h] = (m + __log2f(l)) * 0.69314718055994531f;
+    tc_fence_before();
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int HD>
+__global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using Ly = Layout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Ly::NBAR; ++i)
+      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? 128u : 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k_new);
+    prefetch_tmap(&p.tm_v_new);
+    prefetch_tmap(&p.tm_k_cache);
+    prefetch_tmap(&p.tm_v_cache);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_holder), Ly::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
+
+  if (warp < 4) {
+    softmax_role<HD>(p, sbase, tmem, wait);
+  } else if (warp == 4) {
+    if (lane == 0) producer_role<HD>(p, sbase, wait);
+  } else {
+    if (lane == 0) mma_role<HD>(p, sbase, tmem, wait);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Ly::TMEM_COLS);
+  }
+}
+
+}  // namespace cpattn

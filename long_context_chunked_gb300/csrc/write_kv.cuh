@@ -1,0 +1,57 @@
+// Strided KV-cache write: the chunk's valid tokens, in token order, are
+// copied bit for bit into their striped cache slots (PCP ring-cache PR,
+// Testing section: the strided cache write must be bit-exact; the m-star
+// ring_scatter op has the same pure-copy contract).
+//
+// HBM-bound copy.  One thread moves one 16-byte vector of K and the same
+// vector of V; consecutive threads cover consecutive vectors of one source
+// row, so loads and stores are fully coalesced within each HD*2-byte row.
+#pragma once
+
+#include <cstdint>
+
+#include "walk.cuh"
+
+namespace cpattn {
+
+struct WriteKvParams {
+  const uint4* k_new;
+  const uint4* v_new;
+  uint4* k_cache;
+  uint4* v_cache;
+  int num_seqs, nkv, P, S, C;
+  int vec_per_row;                        // HD * 2 / 16
+  long long total_vecs;                   // sum_b c_b * NKV * vec_per_row
+  int cache_len[CPATTN_MAX_SEQS];
+  long long vec_prefix[CPATTN_MAX_SEQS + 1];  // first vector index of each sequence
+};
+
+__global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ WriteKvParams p) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       idx < p.total_vecs; idx += stride) {
+    // sequence of this vector: binary search in the prefix table
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.vec_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const long long local = idx - p.vec_prefix[b];
+    const long long row = local / p.vec_per_row;          // (i, g) row within the chunk
+    const int vec = static_cast<int>(local - row * p.vec_per_row);
+    const int i = static_cast<int>(row / p.nkv);
+    const int g = static_cast<int>(row - static_cast<long long>(i) * p.nkv);
+    const long long src = (static_cast<long long>(b) * p.C * p.nkv + row) * p.vec_per_row + vec;
+    const int t = p.cache_len[b] + i;
+    const long long dst_row =
+        (static_cast<long long>(b * p.nkv + g) * p.P + (t % p.P)) * p.S + (t / p.P);
+    const long long dst = dst_row * p.vec_per_row + vec;
+    const uint4 kv = __ldg(p.k_new + src);
+    const uint4 vv = __ldg(p.v_new + src);
+    p.k_cache[dst] = kv;
+    p.v_cache[dst] = vv;
+  }
+}
+
+}  // namespace cpattn

@@ -1,0 +1,111 @@
+"""Host-side checks of the C-ABI library: loads, exports every declared symbol,
+validates arguments before any launch, and walks the cache exactly over the
+filled rows of the striped layout.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import long_context_chunked_gb300 as cp
+from long_context_chunked_gb300 import build as cpbuild
+from workloads import ALL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cpbuild.build()
+    return cp.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "cpattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpattn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 9
+    assert sorted(cp.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.cpattn_status_string(s)
+    assert lib.cpattn_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("cfg,status", [
+    ((4, 3, 128, 2, 8, 8), cp.E_INVALID),      # NQ % NKV
+    ((4, 2, 64, 2, 8, 8), cp.E_UNSUPPORTED),   # HD
+    ((4, 2, 128, 0, 8, 8), cp.E_INVALID),      # P
+    ((4, 2, 128, 2, 0, 8), cp.E_INVALID),      # S
+    ((4, 2, 128, 2, 8, 0), cp.E_INVALID),      # C
+])
+def test_create_rejects(lib, cfg, status):
+    with pytest.raises(cp.CpattnError) as e:
+        cp.Context(*cfg)
+    assert e.value.status == status
+
+
+def test_prefill_and_write_validation(lib):
+    ctx = cp.Context(8, 2, 128, 2, 64, 32)
+    A = 256  # a 16-byte-aligned stand-in pointer; nothing is launched
+    good = dict(q=A, k_new=A, v_new=A, k_cache=A, v_cache=A, out=A)
+
+    def pf(cl, ch, **kw):
+        args = dict(good, **kw)
+        return ctx.prefill_raw(cl, ch, args["q"], args["k_new"], args["v_new"], args["k_cache"],
+                               args["v_cache"], args["out"], args.get("lse"), stream=0)
+
+    assert pf([10], [33]) == cp.E_INVALID                 # c > C
+    assert pf([-1], [3]) == cp.E_INVALID                  # L < 0
+    assert pf([120], [9]) == cp.E_INVALID                 # L + c > P*S
+    assert pf([1], [1], q=0) == cp.E_INVALID              # NULL
+    assert pf([1], [1], out=A + 2) == cp.E_INVALID        # misaligned
+    assert pf([1], [1], lse=A + 4) == cp.E_INVALID        # misaligned lse
+    assert pf([], []) == cp.E_INVALID                     # no sequences
+    assert pf([0] * 129, [1] * 129) == cp.E_UNSUPPORTED   # too many sequences
+    assert pf([5], [0]) == cp.OK                          # nothing to do: no launch
+    assert ctx.write_kv_raw([10], [33], A, A, A, A, stream=0) == cp.E_INVALID
+    assert ctx.write_kv_raw([0], [0], A, A, A, A, stream=0) == cp.OK
+    big = cp.Context(8, 2, 128, 1, 1 << 20, 1 << 20)
+    n = 2100 * 128
+    assert big.prefill_raw([0], [n], A, A, A, A, A, A, stream=0) in (cp.E_INVALID, cp.E_UNSUPPORTED)
+
+
+def _filled_rows(L, P, S):
+    fill = oracle.shard_fill(L, P)
+    return {s * S + j for s in range(P) for j in range(int(fill[s]))}
+
+
+WALK_CASES = [(0, 2, 8), (1, 1, 1), (5, 3, 2), (127, 1, 200), (128, 1, 128), (129, 2, 100),
+              (1000, 8, 130), (777, 8, 8013), (60001, 8, 8013), (3000, 8, 8013), (300, 4, 75),
+              (50, 7, 9)] + [(w.cache_lens[0], w.shards, w.shard_capacity) for w in ALL]
+
+
+@pytest.mark.parametrize("L,P,S", WALK_CASES)
+def test_cache_walk_covers_filled_rows_once(lib, L, P, S):
+    ctx = cp.Context(2, 1, 128, P, S, 16)
+    tiles, masks = ctx.cache_walk(L)
+    assert np.all(np.diff(tiles) > 0), "tiles visited in increasing order, each once"
+    seen = set()
+    for t, m in zip(tiles, masks):
+        bits = [(int(m[c // 32]) >> (c % 32)) & 1 for c in range(128)]
+        assert any(bits), "a visited tile has at least one valid column"
+        seen |= {t * 128 + c for c in range(128) if bits[c]}
+    assert seen == _filled_rows(L, P, S)
+
+
+def test_cache_walk_tile_count_is_minimal_for_aligned_shards(lib):
+    # 32k shape: 8 shards of 3584 filled rows, 128-aligned: 224 full tiles.
+    ctx = cp.Context(32, 2, 256, 8, 4096, 4096)
+    tiles, masks = ctx.cache_walk(28672)
+    assert len(tiles) == 224 and np.all(masks == 0xFFFFFFFF)

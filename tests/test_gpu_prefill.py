@@ -1,0 +1,145 @@
+"""Fused prefill on the GPU against the fp64 oracle.
+
+Small cases compare every valid output element; the four full-size
+workloads compare seeded sampled rows (first/last rows of each sequence and
+q block edges included) plus whole-output properties, in the launch
+configuration the benchmark uses.  Bar: max |diff| <= 1e-2 and relative RMS
+<= 2e-3.  Cache holes hold large finite poison; guard bands around every
+buffer must survive."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import long_context_chunked_gb300 as cp
+from gpu_helpers import DeviceCase, compare, to_f64
+from helpers import POISON_BITS, make_case, sample_rows
+from workloads import ALL, CTX_8K, CTX_32K, CTX_128K, TINY, VARLEN, small
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_parity(w, with_lse=True):
+    case = make_case(w)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w)
+    dc.prefill(ctx, with_lse)
+    ref, ref_lse = case.oracle_full()
+    v = dc.valid_rows()
+    out = to_f64(dc.out.bits())
+    res = compare(out[v], ref[v], w.name)
+    if with_lse:
+        lse = dc.lse.cpu().numpy().astype(np.float64)
+        assert np.max(np.abs(lse[v] - ref_lse[v])) < 2e-3, "LSE"
+    # pad rows are never written
+    pad = ~v
+    if pad.any():
+        assert np.all(dc.out.bits()[pad] == np.uint16(0x7F7F)), "pad rows written"
+    assert dc.guards_intact(), "write outside a buffer"
+    return res
+
+
+def test_tiny_full():
+    _full_parity(TINY)
+
+
+EDGE = []
+for hd in (128, 256):
+    for L in (0, 1, 127, 128, 129):
+        for c in (1, 127, 128, 129):
+            EDGE.append(small(f"L{L}c{c}h{hd}", (L,), (c,), 192, nq=4, nkv=2, hd=hd, shards=2,
+                              seed=L * 1000 + c + hd))
+EDGE += [
+    # P in {1, 4, 8}; several tiles per shard; S not a multiple of the tile height
+    small("p1", (300,), (200,), 256, nq=2, nkv=1, hd=128, shards=1, seed=7),
+    small("p4", (1000,), (130,), 256, nq=8, nkv=2, hd=256, shards=4, shard_capacity=300, seed=8),
+    small("p8", (2000,), (64,), 128, nq=4, nkv=4, hd=128, shards=8, shard_capacity=333, seed=9),
+    small("tinyS", (500,), (40,), 64, nq=2, nkv=1, hd=128, shards=8, shard_capacity=70, seed=10),
+    # several sequences with empty, ragged and full chunks
+    small("multi", (0, 50, 700, 129, 256), (300, 0, 17, 256, 128), 300, nq=8, nkv=2, hd=128,
+          shards=4, seed=11),
+    small("multi256", (1, 999, 128), (5, 384, 255), 384, nq=4, nkv=1, hd=256, shards=2,
+          seed=12),
+    small("mha", (333,), (222,), 256, nq=3, nkv=3, hd=128, shards=3, seed=13),
+    small("peaky", (3000,), (500,), 512, nq=8, nkv=2, hd=256, shards=8, seed=14, peaky_frac=0.05),
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=[w.name for w in EDGE])
+def test_edges_full(w):
+    _full_parity(w)
+
+
+FULL = [CTX_8K, CTX_32K, CTX_128K, VARLEN]
+
+
+@pytest.fixture(scope="module")
+def full_runs():
+    return {}
+
+
+@pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
+def test_full_size_sampled(w, full_runs):
+    case = make_case(w)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w)
+    dc.prefill(ctx)
+    samples = sample_rows(w, 48, seed=w.seed)
+    ref, ref_lse = case.oracle_rows(samples)
+    out = to_f64(dc.out.bits())
+    got = np.stack([out[t, h] for t, h in samples])
+    max_abs, rel = compare(got, ref, w.name)
+    lse = dc.lse.cpu().numpy()
+    assert np.max(np.abs(np.array([lse[t, h] for t, h in samples]) - ref_lse)) < 2e-3
+    v = dc.valid_rows()
+    assert np.all(np.isfinite(out[v])), "non-finite output"
+    assert np.all(np.abs(out[v]) < 16), "output outside the convex hull of V"
+    assert dc.guards_intact()
+    # Negative control: the same samples against an oracle given different
+    # cache contents must miss by far more than the passing error.
+    bad = make_case(w.with_(seed=w.seed + 1000))
+    bad.q_bits, bad.k_new_bits, bad.v_new_bits = case.q_bits, case.k_new_bits, case.v_new_bits
+    nref, _ = bad.oracle_rows(samples)
+    neg = float(np.max(np.abs(got - nref)))
+    if sum(w.cache_lens) > 0:
+        assert neg >= 50 * max(max_abs, 1e-4), f"negative control {neg:.3e} vs pass {max_abs:.3e}"
+    full_runs[w.name] = (max_abs, rel, neg)
+
+
+def test_equal_keys_prefix_mean():
+    """All keys equal: every row is the plain mean of its visible values --
+    pins the causal diagonal, the cache visibility and the shard walk."""
+    w = small("eqk", (700, 0), (300, 256), 320, nq=4, nkv=2, hd=128, shards=4,
+              shard_capacity=260, seed=21)
+    case = make_case(w)
+    kvec = case.k_new_bits[0, :, :].copy()
+    case.k_new_bits[...] = kvec[None]
+    case.k_cache_bits[...] = kvec[None, :, None, None, :]
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w)
+    dc.prefill(ctx)
+    out = to_f64(dc.out.bits())
+    vn = case.f64("v_new")
+    G = w.group
+    for b, (L, c) in enumerate(zip(w.cache_lens, w.chunk_lens)):
+        vc = oracle.read_logical(case.f64("v_cache"), b, L)
+        for h in range(w.num_q_heads):
+            g = h // G
+            tot = vc[:, g].sum(axis=0) if L else np.zeros(w.head_dim)
+            run = np.cumsum(vn[b * w.chunk: b * w.chunk + c, g], axis=0)
+            ref = (tot[None] + run) / (L + np.arange(1, c + 1))[:, None]
+            compare(out[b * w.chunk: b * w.chunk + c, h], ref, f"equal keys b={b} h={h}")
+
+
+def test_repeatable_and_write_order_independent():
+    """Two launches give identical bits; running write_kv first changes nothing
+    (prefill reads only cache rows of tokens < L)."""
+    w = small("rep", (900,), (256,), 256, nq=8, nkv=2, hd=256, shards=4, seed=31)
+    case = make_case(w)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w)
+    dc.prefill(ctx)
+    first = dc.out.bits().copy()
+    ctx.write_kv(w.cache_lens, w.chunk_lens, dc.k_new.t, dc.v_new.t, dc.k_cache.t, dc.v_cache.t)
+    dc.prefill(ctx)
+    assert np.array_equal(first, dc.out.bits())
