@@ -1,0 +1,386 @@
+"""Benchmark: one prefill step of chunked-prefill GQA attention on GB300.
+
+A step is the whole hot path over one chunk: the strided KV-cache write of
+the chunk (cpattn_write_kv) and the fused cache+current prefill
+(cpattn_prefill).  The default workload is the 32k-context shape (cache
+28672 + chunk 4096, NQ=32, NKV=2, HD=256, 8 striped shards, 1% of keys
+doubled), seeded synthetic bf16 N(0,1) data.
+
+    python bench.py [--steps K] [--warmup W] [--config 32k] [--gpus N]
+    python bench.py --impl reference      # the CPU oracle on a bounded sample
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an
+independent replica of the workload (no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import BY_NAME, Workload, generate  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "long_context_chunked_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(f"{kernel}:{workload}")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("csrc_hash") != csrc_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ device
+class DeviceState:
+    """Device-resident inputs of one workload: Q and the chunk's K/V in token
+    order, and the striped caches filled with the logical prefix by the
+    library's own KV write."""
+
+    def __init__(self, w: Workload, device, fast_p: bool = False):
+        import torch
+        import long_context_chunked_gb300 as cp
+        self.w = w
+        inp = generate(w)
+        self.inp = inp
+        self.ctx = cp.Context.for_workload(w, fast_p=fast_p)
+        self.q = inp.q.to(device)
+        self.k_new = inp.k_new.to(device)
+        self.v_new = inp.v_new.to(device)
+        shape = (w.num_seqs, w.num_kv_heads, w.shards, w.shard_capacity, w.head_dim)
+        self.k_cache = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.v_cache = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.out = torch.zeros_like(self.q)
+        lmax = max(w.cache_lens)
+        if lmax:
+            fill = cp.Context(w.num_q_heads, w.num_kv_heads, w.head_dim, w.shards,
+                              w.shard_capacity, lmax, w.scale)
+            kl = torch.zeros((w.num_seqs * lmax, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16)
+            vl = torch.zeros_like(kl)
+            for b, L in enumerate(w.cache_lens):
+                kl[b * lmax: b * lmax + L] = inp.k_cache[b]
+                vl[b * lmax: b * lmax + L] = inp.v_cache[b]
+            fill.write_kv([0] * w.num_seqs, list(w.cache_lens), kl.to(device), vl.to(device),
+                          self.k_cache, self.v_cache)
+            fill.close()
+        torch.cuda.synchronize()
+
+    def write_kv(self, stream=None):
+        w = self.w
+        self.ctx.write_kv(w.cache_lens, w.chunk_lens, self.k_new, self.v_new, self.k_cache,
+                          self.v_cache, stream)
+
+    def prefill(self, stream=None):
+        w = self.w
+        self.ctx.prefill(w.cache_lens, w.chunk_lens, self.q, self.k_new, self.v_new,
+                         self.k_cache, self.v_cache, self.out, None, stream)
+
+
+def time_steps(st: DeviceState, steps: int, warmup: int, flush):
+    """Per-step device times (ms) of write_kv + prefill, and of prefill alone,
+    with an L2 flush between steps (outside the timed events)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        st.write_kv()
+        st.prefill()
+    if st.ctx.sync_status() != 0:
+        raise RuntimeError("device status after warm-up: " + st.ctx.last_error())
+    step_ms, prefill_ms = [], []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1, e2 in ev:
+        flush.zero_()
+        e0.record(stream)
+        st.write_kv()
+        e1.record(stream)
+        st.prefill()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    for e0, e1, e2 in ev:
+        step_ms.append(e0.elapsed_time(e2))
+        prefill_ms.append(e1.elapsed_time(e2))
+    if st.ctx.sync_status() != 0:
+        raise RuntimeError("device status after timing: " + st.ctx.last_error())
+    return step_ms, prefill_ms
+
+
+def time_e2e(st: DeviceState, steps: int, warmup: int):
+    """Same step through the public API with inputs in pinned host memory:
+    host->device copy of Q, K_new, V_new, the step, device->host copy of O."""
+    import torch
+    hq = st.inp.q.pin_memory()
+    hk = st.inp.k_new.pin_memory()
+    hv = st.inp.v_new.pin_memory()
+    ho = torch.empty_like(hq).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        st.q.copy_(hq, non_blocking=True)
+        st.k_new.copy_(hk, non_blocking=True)
+        st.v_new.copy_(hv, non_blocking=True)
+        st.write_kv()
+        st.prefill()
+        ho.copy_(st.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+# ------------------------------------------------------------- CPU oracle
+def cpu_sample(w: Workload, budget_rows: int = 384, heads: int = 2):
+    """Time the fp64 oracle, as it stands, on a bounded slice of the workload:
+    the first sequence, `heads` q heads of kv head 0, the first `budget_rows`
+    chunk rows, the full cache.  Returns (TFLOP/s, seconds, description)."""
+    import oracle
+    inp = generate(w)
+    L = w.cache_lens[0]
+    rows = min(budget_rows, w.chunk_lens[0])
+    hd = w.head_dim
+    q = inp.q[:w.chunk, :heads]
+    kn = inp.k_new[:w.chunk, :1]
+    vn = inp.v_new[:w.chunk, :1]
+    kc = oracle.build_striped_cache([oracle.bf16_bits(inp.k_cache[0][:, :1])], 1, w.shards,
+                                    w.shard_capacity, hd, 0)
+    vc = oracle.build_striped_cache([oracle.bf16_bits(inp.v_cache[0][:, :1])], 1, w.shards,
+                                    w.shard_capacity, hd, 0)
+    kcf, vcf = oracle.bits_to_f64(kc), oracle.bits_to_f64(vc)
+    t0 = time.perf_counter()
+    oracle.attend_ref(q, kn, vn, kcf, vcf, [L], [rows], w.chunk, w.scale,
+                      threads=min(heads, os.cpu_count() or 1))
+    dt = time.perf_counter() - t0
+    flops = 4 * hd * heads * (rows * L + rows * (rows + 1) // 2)
+    desc = (f"{w.name}: sequence 0, {heads} q heads of kv head 0, chunk rows 0..{rows - 1}, "
+            f"full cache of {L} tokens ({flops / 1e9:.1f} GFLOP)")
+    return flops / dt / 1e12, dt, desc
+
+
+# ------------------------------------------------------------------- main
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: rank 0 only, bounded samples."""
+    if rank != 0:
+        return
+    w = BY_NAME[args.config]
+    vals = []
+    for _ in range(args.warmup):
+        cpu_sample(w, budget_rows=args.ref_rows)
+    for _ in range(args.steps):
+        tf, dt, desc = cpu_sample(w, budget_rows=args.ref_rows)
+        vals.append((tf, dt))
+    v = statistics.median(t for t, _ in vals)
+    sec = statistics.median(d for _, d in vals)
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 inputs)",
+        "config": {"workload": w.name, "description": w.description},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "fused prefill attention TFLOP/s per chunk (write_kv + prefill) on 1 GB300"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cpattn", choices=["cpattn", "reference"])
+    ap.add_argument("--config", default="32k", choices=sorted(BY_NAME))
+    ap.add_argument("--fast-p", action="store_true", help="P rounded once to bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=384)
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    w = BY_NAME[args.config]
+    st = DeviceState(w, device, fast_p=args.fast_p)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_ms, prefill_ms = time_steps(st, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    e2e_ms, h2d, d2h = time_e2e(st, max(3, args.steps // 2), args.warmup)
+
+    flops = w.attention_flops()
+    ms_step = total_ms / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    pf = statistics.mean(prefill_ms)
+    achieved = flops / (pf * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    kv_ms = statistics.mean(s - p for s, p in zip(step_ms, prefill_ms))
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, 1% of keys doubled)",
+        "config": {"workload": w.name, "description": w.description,
+                   "precision": "fast_p (P rounded to bf16)" if args.fast_p else
+                   "accurate P (bf16 hi+lo pair)",
+                   "l2": "flushed between steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "prefill_ms": round(pf, 4), "write_kv_ms": round(kv_ms, 4),
+        "write_kv_gbs": round(w.kv_write_bytes() / (kv_ms * 1e-3) / 1e9, 1) if kv_ms > 0 else None,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"bf16 dense burst, {peak_kind}",
+                     "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
+                     "kernel": "prefill_kernel<%d>" % w.head_dim,
+                     "traffic": profiled_traffic("prefill", w.name)},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, dt, desc = cpu_sample(w)
+        line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s",
+                                "cores": os.cpu_count() or 1, "kind": "oracle", "sample": desc,
+                                "seconds": round(dt, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -13,7 +13,8 @@ from typing import Optional, Sequence
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libcpattn.so")
+# CPATTN_LIBRARY overrides the library path (e.g. an instrumented build).
+LIB_PATH = os.environ.get("CPATTN_LIBRARY") or os.path.join(_PKG, "libcpattn.so")
 
 OK, E_INVALID, E_UNSUPPORTED, E_CUDA, E_NOMEM, E_TIMEOUT = range(6)
 MAX_SEQS = 128
@@ -35,7 +36,7 @@ class Config(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("num_shards", ctypes.c_int32),
                 ("shard_capacity", ctypes.c_int32), ("chunk_size", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("fast_p", ctypes.c_int32)]
 
 
 _lib = None
@@ -101,10 +102,11 @@ class Context:
     """One attention-layer shape: NQ, NKV, HD, shard count P, shard capacity S, chunk C."""
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, num_shards: int,
-                 shard_capacity: int, chunk_size: int, softmax_scale: float = 0.0):
+                 shard_capacity: int, chunk_size: int, softmax_scale: float = 0.0,
+                 fast_p: bool = False):
         self.lib = load()
         self.cfg = Config(num_q_heads, num_kv_heads, head_dim, num_shards, shard_capacity,
-                          chunk_size, softmax_scale)
+                          chunk_size, softmax_scale, int(bool(fast_p)))
         h = ctypes.c_void_p()
         st = self.lib.cpattn_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if st != OK:
@@ -112,9 +114,9 @@ class Context:
         self._h = h
 
     @classmethod
-    def for_workload(cls, w) -> "Context":
+    def for_workload(cls, w, fast_p: bool = False) -> "Context":
         return cls(w.num_q_heads, w.num_kv_heads, w.head_dim, w.shards, w.shard_capacity,
-                   w.chunk, w.scale)
+                   w.chunk, w.scale, fast_p)
 
     # -- status --------------------------------------------------------
     def _check(self, st: int):

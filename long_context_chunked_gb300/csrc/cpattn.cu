@@ -153,7 +153,7 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   *out = nullptr;
   const cpattn_config& c = *cfg;
   if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
-      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0)
+      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1)
     return CPATTN_E_INVALID;
   if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
   if (c.num_q_heads > 65535) return CPATTN_E_UNSUPPORTED;
@@ -326,6 +326,7 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   prm.S = c.shard_capacity;
   prm.C = c.chunk_size;
   prm.debug_flags = ctx->debug_flags;
+  prm.split_p = c.fast_p ? 0 : 1;
   prm.scale_log2 = c.softmax_scale * 1.4426950408889634f;
   for (int b = 0; b < num_seqs; ++b)
     prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], ncache[b], 0};

@@ -20,9 +20,12 @@
 //              O += P V (P from TMEM, V from shared memory).
 //
 // TMEM (512 columns x 128 lanes, fp32): O at [0, HD), S double buffer at
-// [HD, HD+128) and [HD+128, HD+256).  P_t is written over the first 64
-// columns of its S buffer; MMAs of one thread execute in issue order, so the
-// QK^T that next overwrites that buffer (tile t+2) runs after PV_t read P_t.
+// [HD, HD+128) and [HD+128, HD+256).  P_t (bf16, two per column) is written
+// over its S buffer: the bf16 rounding of p in columns [0, 64) and, in the
+// accurate mode, the bf16 rounding of the remainder p - hi in [64, 128); O
+// then takes two products P_hi V + P_lo V, which carries p to ~16 bits.
+// MMAs of one thread execute in issue order, so the QK^T that next
+// overwrites that buffer (tile t+2) runs after PV_t read P_t.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -48,6 +51,7 @@ struct PrefillParams {
   int* status;
   unsigned long long timeout_ns;
   int num_units, nq, nkv, group, P, S, C, debug_flags;
+  int split_p;  // 1: P as bf16 hi + lo pair (two PV products); 0: P rounded to bf16
   float scale_log2;
   SeqInfo seqs[CPATTN_MAX_SEQS];
   uint32_t blocks[CPATTN_MAX_ROW_BLOCKS];  // (b << 16) | q block, longest first
@@ -231,8 +235,9 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
       for (int kk = 0; kk < Ly::VROWS / 16; ++kk) {
         // V sub-tile: KCH column chunks of VROWS rows x 128 B, N-contiguous.
         const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, Ly::VROWS * 128, 1024);
-        mma_ts(tmem, p_tmem + (j * Ly::VROWS + kk * 16) / 2, bd, Ly::IDESC_PV,
-               (w | j | kk) != 0);
+        const uint32_t pa = p_tmem + (j * Ly::VROWS + kk * 16) / 2;
+        mma_ts(tmem, pa, bd, Ly::IDESC_PV, (w | j | kk) != 0);
+        if (p.split_p) mma_ts(tmem, pa + kBKV / 2, bd, Ly::IDESC_PV, 1u);
       }
       mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
       rp.template advance<Ly::NSLOT>();
@@ -357,19 +362,48 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       }
       const float m_tile = fmaxf(fmaxf(mt0, mt1), fmaxf(mt2, mt3)) * sl2;
       const float m_new = fmaxf(m, m_tile);
-      if (v == 0) {
-        m = m_new;
-      } else {
-        // Lazy rescale: keep the old reference max unless the new one exceeds
-        // it by more than 2^8; the final O / l is the same either way.
-        const bool need = m_new > m + 8.f;
-        if (__any_sync(0xFFFFFFFFu, need)) {
-          const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-          if (need) m = m_new;
-          ok = wait(bar(Ly::B_ODONE), (tile_ctr - 1) & 1u, kSiteODone);  // PV of tile t-1
-          ok = __all_sync(0xFFFFFFFFu, ok);
-          if (!ok) break;
-          tc_fence_after();
+      // Lazy rescale: keep the old reference max unless the new one exceeds
+      // it by more than 2^8; the final O / l is the same either way.
+      const bool need = (v > 0) && (m_new > m + 8.f);
+      const bool warp_rescale = __any_sync(0xFFFFFFFFu, need);
+      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+      if (v == 0 || need) m = m_new;
+
+      // p = 2^(x - m) and the row sum; P_hi = bf16(p) into columns [0, 64) of
+      // the S buffer and, in the accurate mode, P_lo = bf16(p - P_hi) into
+      // columns [64, 128).  Written 32 probabilities at a time.
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = ex2_approx(fmaf(s[32 * q + 2 * i], sl2, neg_m));
+          const float b = ex2_approx(fmaf(s[32 * q + 2 * i + 1], sl2, neg_m));
+          l0 += a;
+          l1 += b;
+          hi[i] = pack_bf16x2(a, b);
+          lo[i] = pack_bf16x2(a - __uint_as_float(hi[i] << 16),
+                              b - __uint_as_float(hi[i] & 0xFFFF0000u));
+        }
+        tmem_st16(s_tmem + 16 * q, hi);
+        if (p.split_p) tmem_st16(s_tmem + kBKV / 2 + 16 * q, lo);
+      }
+      l = l * alpha + (l0 + l1);
+
+      // Observe the completion of PV of the previous tile (global index
+      // tile_ctr - 1) before releasing P of this one.  Every PV completion is
+      // observed in order: an mbarrier parity wait is unambiguous only while
+      // the waiter is at most one phase behind, and PV of this tile cannot
+      // start before this thread's arrival below.  The first tile of a unit
+      // skips it: the previous unit's epilogue observed that completion.
+      if (v > 0) {
+        ok = wait(bar(Ly::B_ODONE), (tile_ctr - 1) & 1u, kSiteODone);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (warp_rescale) {
 #pragma unroll 1
           for (int ch = 0; ch < HD / 32; ++ch) {
             uint32_t o[32];
@@ -378,34 +412,8 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st32(lane_tmem + 32 * ch, o);
           }
-          tmem_wait_st();
-          l *= alpha;
         }
       }
-
-      // p = 2^(x - m), row sum, bf16 pack into the first 64 columns of S.
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float l0 = 0.f, l1 = 0.f;
-      uint32_t pk0[32], pk1[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = ex2_approx(fmaf(s[2 * i], sl2, neg_m));
-        const float b = ex2_approx(fmaf(s[2 * i + 1], sl2, neg_m));
-        l0 += a;
-        l1 += b;
-        pk0[i] = pack_bf16x2(a, b);
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = ex2_approx(fmaf(s[64 + 2 * i], sl2, neg_m));
-        const float b = ex2_approx(fmaf(s[64 + 2 * i + 1], sl2, neg_m));
-        l0 += a;
-        l1 += b;
-        pk1[i] = pack_bf16x2(a, b);
-      }
-      l += l0 + l1;
-      tmem_st32(s_tmem, pk0);
-      tmem_st32(s_tmem + 32, pk1);
       tmem_wait_st();
       tc_fence_before();
       if (drop_one) {

@@ -36,16 +36,26 @@ def to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
 def compare(out: np.ndarray, ref: np.ndarray, what: str = ""):
-    """Parity bar: max |diff| <= 1e-2 and relative RMS <= 2e-3 (bf16 output,
-    fp32 accumulation, against the unrounded fp64 oracle)."""
+    """Parity bar against the unrounded fp64 oracle: relative RMS <= 2e-3 and
+    max |diff| <= 1e-2.  Where rounding the exact value to bf16 alone moves it
+    by more than half that bar (|O| >= 4, half-ulp 1.6e-2), the element may
+    also differ by its own rounding error plus 5e-3: no bf16 output can do
+    better there."""
     assert out.shape == ref.shape, (out.shape, ref.shape)
     assert np.all(np.isfinite(out)), f"{what}: non-finite output"
     d = out - ref
+    rounding = np.abs(bf16_round(ref) - ref)
+    allowed = np.maximum(MAX_ABS, rounding + MAX_ABS / 2)
+    excess = float(np.max(np.abs(d) - allowed))
     max_abs = float(np.max(np.abs(d)))
     rel = float(np.sqrt(np.sum(d * d) / np.sum(ref * ref)))
-    assert max_abs <= MAX_ABS and rel <= MAX_REL_RMS, \
-        f"{what}: max|d|={max_abs:.3e} (<= {MAX_ABS}), relRMS={rel:.3e} (<= {MAX_REL_RMS})"
+    assert excess <= 0 and rel <= MAX_REL_RMS, \
+        f"{what}: max|d|={max_abs:.3e} (<= {MAX_ABS} + rounding), relRMS={rel:.3e} (<= {MAX_REL_RMS})"
     return max_abs, rel
 
 
