@@ -150,6 +150,41 @@ cpattn_status cpattn_set_fault_injection(cpattn_ctx* ctx, int32_t flags, int32_t
 cpattn_status cpattn_cache_walk(const cpattn_ctx* ctx, int32_t cache_len, int32_t* tiles,
                                 uint32_t* masks, int32_t max_tiles, int32_t* count);
 
+/*
+ * Allocation-free fused prefill.  The pages have no counterpart for this
+ * entry point; it exists for callers that cannot allocate device memory --
+ * code running while a pooled or custom allocator owns the device, regions
+ * where cudaMalloc/cudaFree are forbidden or would synchronise (for example
+ * while a stream is being captured), embedders that only pass pointers in.
+ *
+ * Same computation, arguments and layouts as cpattn_prefill, but it takes
+ * the configuration directly instead of a context and never allocates: no
+ * cudaMalloc, no cudaFree, no allocating library call, no host heap.  The
+ * kernel's bounded-wait status word lives in a file-scope device array of
+ * CPATTN_NOALLOC_SCRATCH_INTS ints (256 bytes) that every GPU loading the
+ * library keeps until process exit.
+ *  - The first call on a device resolves that array's device address and
+ *    sets the kernel attributes for that device (with that device current);
+ *    make that first call before any stream capture on the device.
+ *  - Every call shares the array and clears the status word on `stream`
+ *    before its launch.  Calls that overlap on the GPU (other streams, other
+ *    threads) race on it; serialise them.
+ *  - A device-side wait that expires still ends the kernel early (outputs
+ *    incomplete) but is not reported by this call.
+ *  - Sizes beyond the fixed host tables are refused: num_seqs >
+ *    CPATTN_MAX_SEQS or more than CPATTN_MAX_ROW_BLOCKS row blocks return
+ *    CPATTN_E_UNSUPPORTED, as do more than 64 devices.
+ * Errors: E_INVALID (bad configuration or arguments, as for cpattn_create and
+ * cpattn_prefill, or a buffer pointer the driver does not know as device or
+ * managed memory), E_UNSUPPORTED (limits above), E_CUDA (set-up or launch).
+ */
+#define CPATTN_NOALLOC_SCRATCH_INTS 64
+cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_t num_seqs,
+                                     const int32_t* cache_lens, const int32_t* chunk_lens,
+                                     const void* q, const void* k_new, const void* v_new,
+                                     const void* k_cache, const void* v_cache, void* out,
+                                     float* lse, void* stream);
+
 /* Free the context (NULL-safe).  Does not synchronise. */
 void cpattn_destroy(cpattn_ctx* ctx);
 

@@ -23,7 +23,7 @@ MAX_ROW_BLOCKS = 2048
 # Every symbol include/cpattn.h declares.
 EXPORTS = ("cpattn_create", "cpattn_write_kv", "cpattn_prefill", "cpattn_sync_status",
            "cpattn_set_fault_injection", "cpattn_cache_walk", "cpattn_destroy",
-           "cpattn_status_string", "cpattn_last_error")
+           "cpattn_status_string", "cpattn_last_error", "cpattn_prefill_noalloc")
 
 
 class CpattnError(RuntimeError):
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cpattn_status_string.restype = ctypes.c_char_p
     lib.cpattn_last_error.argtypes = [P]
     lib.cpattn_last_error.restype = ctypes.c_char_p
+    lib.cpattn_prefill_noalloc.argtypes = [ctypes.POINTER(Config), I32, I32P, I32P] + [P] * 8
+    lib.cpattn_prefill_noalloc.restype = I32
     _lib = lib
     return lib
 
@@ -194,3 +196,15 @@ class Context:
                 continue
             if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
                 raise ValueError("expected contiguous bf16 CUDA tensors")
+
+
+def prefill_noalloc(cfg: Config, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out,
+                    lse=None, stream=None) -> int:
+    """cpattn_prefill_noalloc: the fused prefill without a context and without
+    any allocation, for callers that cannot allocate device memory.  Returns
+    the status code."""
+    fn = load().cpattn_prefill_noalloc
+    cl, clp = _i32(cache_lens)
+    ch, chp = _i32(chunk_lens)
+    return fn(ctypes.byref(cfg), len(cl), clp, chp, _ptr(q), _ptr(k_new), _ptr(v_new),
+              _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), _stream(stream))

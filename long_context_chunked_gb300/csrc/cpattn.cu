@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -339,3 +340,175 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free prefill.  Some callers must not allocate device memory at
+// all: code that runs while a custom or pooled allocator owns the device,
+// code inside a region where cudaMalloc/cudaFree would synchronise the device
+// or are forbidden (for instance while a stream is being captured), and
+// embedders that only hand over input and output pointers.  The context-based
+// cpattn_prefill needs cpattn_create, which cudaMalloc's the kernel's status
+// word; this entry point instead keeps that scratch word in the file-scope
+// array below, which every GPU that loads the library holds until exit.
+
+// Scratch of the allocation-free path: word 0 is the prefill kernel's
+// bounded-wait status word.  256 bytes per device.
+static __device__ __align__(256) int g_noalloc_scratch[CPATTN_NOALLOC_SCRATCH_INTS];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready = false;
+  int* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+};
+
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Once per device, with that device current: resolve the device address of
+// the scratch array (its host-side name is only a stand-in) and set the
+// kernels' shared-memory attribute.
+cpattn_status noalloc_setup(NoAllocDevice** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return CPATTN_E_CUDA;
+  if (dev >= kNoAllocMaxDevices) return CPATTN_E_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    int* ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch) != cudaSuccess ||
+        ptr == nullptr)
+      return CPATTN_E_CUDA;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return CPATTN_E_CUDA;
+    if (cudaFuncSetAttribute(cpattn::prefill_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             cpattn::Layout<128>::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(cpattn::prefill_kernel<256>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             cpattn::Layout<256>::SMEM_BYTES) != cudaSuccess)
+      return CPATTN_E_CUDA;
+    d.scratch = ptr;
+    d.ready = true;
+  }
+  *out = &d;
+  return CPATTN_OK;
+}
+
+// True iff p is device (or managed) memory known to the driver; a host or
+// truncated address is refused before it can reach a kernel.
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace
+
+extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_t num_seqs,
+                                                const int32_t* cache_lens,
+                                                const int32_t* chunk_lens, const void* q,
+                                                const void* k_new, const void* v_new,
+                                                const void* k_cache, const void* v_cache,
+                                                void* out, float* lse, void* stream) {
+  if (cfg == nullptr) return CPATTN_E_INVALID;
+  const cpattn_config& c = *cfg;
+  if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
+      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1)
+    return CPATTN_E_INVALID;
+  if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
+  // Fixed-capacity host tables: sizes beyond them are refused, not grown.
+  if (num_seqs < 1) return CPATTN_E_INVALID;
+  if (num_seqs > CPATTN_MAX_SEQS) return CPATTN_E_UNSUPPORTED;
+  if (cache_lens == nullptr || chunk_lens == nullptr || q == nullptr || k_new == nullptr ||
+      v_new == nullptr || k_cache == nullptr || v_cache == nullptr || out == nullptr)
+    return CPATTN_E_INVALID;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)))
+    return CPATTN_E_INVALID;
+  const long long cap = static_cast<long long>(c.num_shards) * c.shard_capacity;
+  int nblk = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    if (cache_lens[b] < 0 || chunk_lens[b] < 0 || chunk_lens[b] > c.chunk_size ||
+        static_cast<long long>(cache_lens[b]) + chunk_lens[b] > cap)
+      return CPATTN_E_INVALID;
+    nblk += (chunk_lens[b] + kBQ - 1) / kBQ;
+  }
+  if (nblk > CPATTN_MAX_ROW_BLOCKS) return CPATTN_E_UNSUPPORTED;
+  const long long cache_rows =
+      static_cast<long long>(num_seqs) * c.num_kv_heads * c.num_shards * c.shard_capacity;
+  if (cache_rows + kBKV >= (1LL << 31) ||
+      static_cast<long long>(num_seqs) * c.chunk_size + kBQ >= (1LL << 31))
+    return CPATTN_E_UNSUPPORTED;
+  if (nblk == 0) return CPATTN_OK;
+
+  NoAllocDevice* dev = nullptr;
+  cpattn_status s = noalloc_setup(&dev);
+  if (s != CPATTN_OK) return s;
+  if (!is_device_ptr(q) || !is_device_ptr(k_new) || !is_device_ptr(v_new) ||
+      !is_device_ptr(k_cache) || !is_device_ptr(v_cache) || !is_device_ptr(out) ||
+      (lse != nullptr && !is_device_ptr(lse)))
+    return CPATTN_E_INVALID;
+
+  static thread_local cpattn::PrefillParams prm;
+  static thread_local uint64_t keys[CPATTN_MAX_ROW_BLOCKS];
+  std::memset(&prm, 0, sizeof(prm));
+  // Row blocks longest first (ties by sequence, then block), without a heap.
+  int n = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    const int ncache = cpattn::cache_tile_count(cache_lens[b], c.num_shards, c.shard_capacity);
+    prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], ncache, 0};
+    const int nqb = (chunk_lens[b] + kBQ - 1) / kBQ;
+    for (int qb = 0; qb < nqb; ++qb) {
+      const uint64_t work = static_cast<uint64_t>(ncache + qb + 1);
+      keys[n++] = ((0xFFFFFFFFull - work) << 32) | (static_cast<uint64_t>(b) << 16) |
+                  static_cast<uint64_t>(qb);
+    }
+  }
+  std::sort(keys, keys + n);
+  for (int i = 0; i < n; ++i) prm.blocks[i] = static_cast<uint32_t>(keys[i] & 0xFFFFFFFFull);
+
+  const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
+  const uint64_t T = static_cast<uint64_t>(num_seqs) * c.chunk_size;
+  const uint64_t rows = static_cast<uint64_t>(cache_rows);
+  const uint32_t vrows = 8192u / static_cast<uint32_t>(HD);
+  const uint64_t rb = static_cast<uint64_t>(HD) * 2;
+  if (!(encode3d(&prm.tm_q, q, HD, NQ, T, rb, rb * NQ, 64, 1, kBQ) &&
+        encode3d(&prm.tm_k_new, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV) &&
+        encode3d(&prm.tm_v_new, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, vrows) &&
+        encode3d(&prm.tm_k_cache, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV) &&
+        encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows)))
+    return CPATTN_E_CUDA;
+  const float scale = c.softmax_scale > 0.f ? c.softmax_scale
+                                            : 1.0f / std::sqrt(static_cast<float>(HD));
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.status = dev->scratch;
+  prm.timeout_ns = 1000ull * 1000 * 1000;
+  prm.nq = NQ;
+  prm.nkv = NKV;
+  prm.group = NQ / NKV;
+  prm.P = c.num_shards;
+  prm.S = c.shard_capacity;
+  prm.C = c.chunk_size;
+  prm.debug_flags = 0;
+  prm.split_p = c.fast_p ? 0 : 1;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.num_units = n * NQ;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status word must start at zero; the previous call's value is stale.
+  if (cudaMemsetAsync(dev->scratch, 0, sizeof(int), st) != cudaSuccess) return CPATTN_E_CUDA;
+  const int grid = std::min(prm.num_units, dev->num_sms);
+  if (HD == 256)
+    cpattn::prefill_kernel<256><<<grid, 192, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+  else
+    cpattn::prefill_kernel<128><<<grid, 192, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_E_CUDA;
+}

@@ -36,6 +36,16 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_every_export_has_a_typed_binding(lib):
+    """ctypes defaults to 32-bit int arguments: an entry point called without
+    argtypes would truncate device pointers.  Every symbol must be typed."""
+    for n in cp.EXPORTS:
+        fn = getattr(lib, n)
+        if n != "cpattn_destroy":
+            assert fn.restype is not None, n
+        assert fn.argtypes is not None and len(fn.argtypes) >= 1, n
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert lib.cpattn_status_string(s)
