@@ -24,7 +24,7 @@ struct cpattn_ctx {
   int device = -1;
   int num_sms = 0;
   int* d_status = nullptr;           // device status word (timeouts)
-  bool attr_set_128 = false, attr_set_256 = false;
+  bool attr_set[2][2] = {{false, false}, {false, false}};  // [HD == 256][split P]
   int debug_flags = 0;
   unsigned long long timeout_ns = 1000ull * 1000 * 1000;
   bool debug_sync = false;
@@ -113,19 +113,19 @@ cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* wha
   return CPATTN_OK;
 }
 
-template <int HD>
+template <int HD, bool SPLIT>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
   using Ly = cpattn::Layout<HD>;
-  bool& attr = HD == 256 ? ctx->attr_set_256 : ctx->attr_set_128;
+  bool& attr = ctx->attr_set[HD == 256][SPLIT];
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(cpattn::prefill_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(cpattn::prefill_kernel<HD, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Ly::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(prefill)");
     attr = true;
   }
   const int grid = std::min(prm->num_units, ctx->num_sms);
-  cpattn::prefill_kernel<HD><<<grid, 192, Ly::SMEM_BYTES, stream>>>(*prm);
+  cpattn::prefill_kernel<HD, SPLIT><<<grid, 192, Ly::SMEM_BYTES, stream>>>(*prm);
   return after_launch(ctx, stream, "prefill launch");
 }
 
@@ -327,7 +327,6 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   prm.S = c.shard_capacity;
   prm.C = c.chunk_size;
   prm.debug_flags = ctx->debug_flags;
-  prm.split_p = c.fast_p ? 0 : 1;
   prm.scale_log2 = c.softmax_scale * 1.4426950408889634f;
   for (int b = 0; b < num_seqs; ++b)
     prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], ncache[b], 0};
@@ -336,7 +335,10 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   prm.num_units = static_cast<int>(blks.size()) * NQ;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return HD == 256 ? launch_prefill<256>(ctx, &prm, st) : launch_prefill<128>(ctx, &prm, st);
+  const bool split = c.fast_p == 0;
+  if (HD == 256)
+    return split ? launch_prefill<256, true>(ctx, &prm, st) : launch_prefill<256, false>(ctx, &prm, st);
+  return split ? launch_prefill<128, true>(ctx, &prm, st) : launch_prefill<128, false>(ctx, &prm, st);
 }
 
 }  // extern "C"
@@ -384,10 +386,16 @@ cpattn_status noalloc_setup(NoAllocDevice** out) {
       return CPATTN_E_CUDA;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return CPATTN_E_CUDA;
-    if (cudaFuncSetAttribute(cpattn::prefill_kernel<128>,
+    if (cudaFuncSetAttribute(cpattn::prefill_kernel<128, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              cpattn::Layout<128>::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn::prefill_kernel<256>,
+        cudaFuncSetAttribute(cpattn::prefill_kernel<128, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             cpattn::Layout<128>::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(cpattn::prefill_kernel<256, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             cpattn::Layout<256>::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(cpattn::prefill_kernel<256, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              cpattn::Layout<256>::SMEM_BYTES) != cudaSuccess)
       return CPATTN_E_CUDA;
@@ -498,7 +506,6 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   prm.S = c.shard_capacity;
   prm.C = c.chunk_size;
   prm.debug_flags = 0;
-  prm.split_p = c.fast_p ? 0 : 1;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.num_units = n * NQ;
 
@@ -506,9 +513,14 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   // The status word must start at zero; the previous call's value is stale.
   if (cudaMemsetAsync(dev->scratch, 0, sizeof(int), st) != cudaSuccess) return CPATTN_E_CUDA;
   const int grid = std::min(prm.num_units, dev->num_sms);
-  if (HD == 256)
-    cpattn::prefill_kernel<256><<<grid, 192, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+  const bool split = c.fast_p == 0;
+  if (HD == 256 && split)
+    cpattn::prefill_kernel<256, true><<<grid, 192, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+  else if (HD == 256)
+    cpattn::prefill_kernel<256, false><<<grid, 192, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+  else if (split)
+    cpattn::prefill_kernel<128, true><<<grid, 192, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
   else
-    cpattn::prefill_kernel<128><<<grid, 192, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<128, false><<<grid, 192, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_E_CUDA;
 }

@@ -21,9 +21,10 @@
 //
 // TMEM (512 columns x 128 lanes, fp32): O at [0, HD), S double buffer at
 // [HD, HD+128) and [HD+128, HD+256).  P_t (bf16, two per column) is written
-// over its S buffer: the bf16 rounding of p in columns [0, 64) and, in the
-// accurate mode, the bf16 rounding of the remainder p - hi in [64, 128); O
-// then takes two products P_hi V + P_lo V, which carries p to ~16 bits.
+// over its S buffer, per 32-key chunk over that chunk's own 32 columns: the
+// bf16 rounding P_hi of p in the first 16 and, in the accurate mode (SPLIT),
+// the bf16 rounding P_lo of the remainder p - P_hi in the next 16; O then
+// takes two products P_hi V + P_lo V, which carries p to ~16 bits.
 // MMAs of one thread execute in issue order, so the QK^T that next
 // overwrites that buffer (tile t+2) runs after PV_t read P_t.
 #pragma once
@@ -51,7 +52,6 @@ struct PrefillParams {
   int* status;
   unsigned long long timeout_ns;
   int num_units, nq, nkv, group, P, S, C, debug_flags;
-  int split_p;  // 1: P as bf16 hi + lo pair (two PV products); 0: P rounded to bf16
   float scale_log2;
   SeqInfo seqs[CPATTN_MAX_SEQS];
   uint32_t blocks[CPATTN_MAX_ROW_BLOCKS];  // (b << 16) | q block, longest first
@@ -210,7 +210,7 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
 }
 
 // ------------------------------------------------------------- MMA issuer
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                          const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -235,9 +235,12 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
       for (int kk = 0; kk < Ly::VROWS / 16; ++kk) {
         // V sub-tile: KCH column chunks of VROWS rows x 128 B, N-contiguous.
         const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, Ly::VROWS * 128, 1024);
-        const uint32_t pa = p_tmem + (j * Ly::VROWS + kk * 16) / 2;
+        // P of key rows e0..e0+15: chunk e0/32, 8 packed columns at
+        // (e0 % 32) / 2 within the chunk's hi half; its lo half follows.
+        const int e0 = j * Ly::VROWS + kk * 16;
+        const uint32_t pa = p_tmem + 32 * (e0 >> 5) + ((e0 & 31) >> 1);
         mma_ts(tmem, pa, bd, Ly::IDESC_PV, (w | j | kk) != 0);
-        if (p.split_p) mma_ts(tmem, pa + kBKV / 2, bd, Ly::IDESC_PV, 1u);
+        if (SPLIT) mma_ts(tmem, pa + 16, bd, Ly::IDESC_PV, 1u);
       }
       mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
       rp.template advance<Ly::NSLOT>();
@@ -300,7 +303,7 @@ __device__ __forceinline__ uint32_t causal_word(int lim, int q) {
 }
 
 // ------------------------------------------------------- softmax + epilogue
-template <int HD>
+template <int HD, bool SPLIT>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                              const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -326,16 +329,8 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       if (!ok) break;
       tc_fence_after();
       const uint32_t s_tmem = lane_tmem + HD + sb * kBKV;
-      float s[kBKV];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t raw[32];
-        tmem_ld32_wait(s_tmem + 32 * q, raw);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * q + i] = __uint_as_float(raw[i]);
-      }
 
-      // Region by value: one scalar picks the validity words.
+      // Region by value: one scalar picks the validity words of the tile.
       const bool in_cache = v < U.n_cache;
       uint32_t mw[4];
       if (in_cache) {
@@ -345,22 +340,45 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 #pragma unroll
         for (int q = 0; q < 4; ++q) mw[q] = causal_word(lim, q);
       }
-      const bool need_mask = __any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < kBKV; ++c)
-          s[c] = ((mw[c >> 5] >> (c & 31)) & 1u) ? s[c] : -INFINITY;
-      }
+      const bool need_mask =
+          __any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu);
 
-      float mt0 = s[0], mt1 = s[1], mt2 = s[2], mt3 = s[3];
+      // Pass 1: row max of the logits, streamed from TMEM 32 columns at a
+      // time (next chunk's load in flight).  On a partly masked tile the
+      // masked logits are written back as -inf, so pass 2 carries no mask.
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      {
+        uint32_t ra[32], rb[32];
+        auto chunk_max = [&](uint32_t (&x)[32], uint32_t word, int q) {
+          if (need_mask) {
 #pragma unroll
-      for (int c = 4; c < kBKV; c += 4) {
-        mt0 = fmaxf(mt0, s[c]);
-        mt1 = fmaxf(mt1, s[c + 1]);
-        mt2 = fmaxf(mt2, s[c + 2]);
-        mt3 = fmaxf(mt3, s[c + 3]);
+            for (int i = 0; i < 32; ++i)
+              x[i] = ((word >> i) & 1u) ? x[i] : 0xFF800000u;  // -inf
+            tmem_st32(s_tmem + 32 * q, x);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            mx0 = fmaxf(mx0, __uint_as_float(x[i]));
+            mx1 = fmaxf(mx1, __uint_as_float(x[i + 1]));
+            mx2 = fmaxf(mx2, __uint_as_float(x[i + 2]));
+            mx3 = fmaxf(mx3, __uint_as_float(x[i + 3]));
+          }
+        };
+        tmem_ld32_async(s_tmem, ra);
+        tmem_ld32_fence(ra);
+        tmem_ld32_async(s_tmem + 32, rb);
+        chunk_max(ra, mw[0], 0);
+        tmem_ld32_fence(rb);
+        tmem_ld32_async(s_tmem + 64, ra);
+        chunk_max(rb, mw[1], 1);
+        tmem_ld32_fence(ra);
+        tmem_ld32_async(s_tmem + 96, rb);
+        chunk_max(ra, mw[2], 2);
+        tmem_ld32_fence(rb);
+        chunk_max(rb, mw[3], 3);
+        if (need_mask) tmem_wait_st();
       }
-      const float m_tile = fmaxf(fmaxf(mt0, mt1), fmaxf(mt2, mt3)) * sl2;
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       const float m_new = fmaxf(m, m_tile);
       // Lazy rescale: keep the old reference max unless the new one exceeds
       // it by more than 2^8; the final O / l is the same either way.
@@ -369,28 +387,48 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       const float alpha = need ? ex2_approx(m - m_new) : 1.f;
       if (v == 0 || need) m = m_new;
 
-      // p = 2^(x - m) and the row sum; P_hi = bf16(p) into columns [0, 64) of
-      // the S buffer and, in the accurate mode, P_lo = bf16(p - P_hi) into
-      // columns [64, 128).  Written 32 probabilities at a time.
+      // Pass 2: p = 2^(x - m) and the row sum.  Chunk q (32 columns) holds,
+      // over its own 32 columns of the S buffer, P_hi = bf16(p) in the first
+      // 16 and -- accurate mode -- P_lo = bf16(p - P_hi) in the next 16.
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      float l0 = 0.f, l1 = 0.f;
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 negm2 = make_float2(neg_m, neg_m);
+      const float2 minus1 = make_float2(-1.f, -1.f);
+      float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
+      {
+        uint32_t ra[32], rb[32];
+        auto chunk_exp = [&](const uint32_t (&x)[32], int q) {
+          uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = ex2_approx(fmaf(s[32 * q + 2 * i], sl2, neg_m));
-          const float b = ex2_approx(fmaf(s[32 * q + 2 * i + 1], sl2, neg_m));
-          l0 += a;
-          l1 += b;
-          hi[i] = pack_bf16x2(a, b);
-          lo[i] = pack_bf16x2(a - __uint_as_float(hi[i] << 16),
-                              b - __uint_as_float(hi[i] & 0xFFFF0000u));
+          for (int i = 0; i < 16; ++i) {
+            const float2 y = __ffma2_rn(
+                make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), sl2x2,
+                negm2);
+            const float2 pab = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+            if (i & 1) lsb = __fadd2_rn(lsb, pab); else lsa = __fadd2_rn(lsa, pab);
+            hi[i] = pack_bf16x2(pab.x, pab.y);
+            if (SPLIT) {
+              const float2 hf = make_float2(__uint_as_float(hi[i] << 16),
+                                            __uint_as_float(hi[i] & 0xFFFF0000u));
+              const float2 res = __ffma2_rn(hf, minus1, pab);
+              lo[i] = pack_bf16x2(res.x, res.y);
+            }
+          }
+          tmem_st16(s_tmem + 32 * q, hi);
+          if (SPLIT) tmem_st16(s_tmem + 32 * q + 16, lo);
+        };
+        tmem_ld32_async(s_tmem, ra);
+#pragma unroll 1
+        for (int q = 0; q < 4; q += 2) {
+          tmem_ld32_fence(ra);
+          tmem_ld32_async(s_tmem + 32 * (q + 1), rb);
+          chunk_exp(ra, q);
+          tmem_ld32_fence(rb);
+          if (q + 2 < 4) tmem_ld32_async(s_tmem + 32 * (q + 2), ra);
+          chunk_exp(rb, q + 1);
         }
-        tmem_st16(s_tmem + 16 * q, hi);
-        if (p.split_p) tmem_st16(s_tmem + kBKV / 2 + 16 * q, lo);
       }
-      l = l * alpha + (l0 + l1);
+      l = l * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
       // Observe the completion of PV of the previous tile (global index
       // tile_ctr - 1) before releasing P of this one.  Every PV completion is
@@ -457,7 +495,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 }
 
 // ------------------------------------------------------------------ kernel
-template <int HD>
+template <int HD, bool SPLIT>
 __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -493,11 +531,11 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
   const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
 
   if (warp < 4) {
-    softmax_role<HD>(p, sbase, tmem, wait);
+    softmax_role<HD, SPLIT>(p, sbase, tmem, wait);
   } else if (warp == 4) {
     if (lane == 0) producer_role<HD>(p, sbase, wait);
   } else {
-    if (lane == 0) mma_role<HD>(p, sbase, tmem, wait);
+    if (lane == 0) mma_role<HD, SPLIT>(p, sbase, tmem, wait);
   }
   __syncwarp();
   tc_fence_before();
