@@ -125,7 +125,7 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
     attr = true;
   }
   const int grid = std::min(prm->num_units, ctx->num_sms);
-  cpattn::prefill_kernel<HD, SPLIT><<<grid, 192, Ly::SMEM_BYTES, stream>>>(*prm);
+  cpattn::prefill_kernel<HD, SPLIT><<<grid, cpattn::kThreads, Ly::SMEM_BYTES, stream>>>(*prm);
   return after_launch(ctx, stream, "prefill launch");
 }
 
@@ -208,8 +208,9 @@ cpattn_status cpattn_cache_walk(const cpattn_ctx* ctx, int32_t cache_len, int32_
     if ((tiles != nullptr || masks != nullptr) && n >= max_tiles) return CPATTN_E_INVALID;
     if (tiles != nullptr) tiles[n] = t;
     if (masks != nullptr) {
-      uint32_t mw[4];
-      w.column_mask(t, mw);
+      // Same decision as the prefill kernel: interior tiles are full.
+      uint32_t mw[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+      if (!w.last_full) w.column_mask(t, mw);
       std::memcpy(masks + 4 * n, mw, sizeof(mw));
     }
     ++n;
@@ -515,12 +516,12 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   const int grid = std::min(prm.num_units, dev->num_sms);
   const bool split = c.fast_p == 0;
   if (HD == 256 && split)
-    cpattn::prefill_kernel<256, true><<<grid, 192, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<256, true><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
   else if (HD == 256)
-    cpattn::prefill_kernel<256, false><<<grid, 192, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<256, false><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
   else if (split)
-    cpattn::prefill_kernel<128, true><<<grid, 192, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<128, true><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
   else
-    cpattn::prefill_kernel<128, false><<<grid, 192, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<128, false><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_E_CUDA;
 }

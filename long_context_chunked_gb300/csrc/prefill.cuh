@@ -9,13 +9,14 @@
 // is selected by the value of one scalar (in_cache = v < n_cache): it picks
 // the tensor map and coordinates of the tile loads and the column mask.
 //
-// Roles (192 threads):
-//   warps 0-3  softmax: tcgen05.ld S row-per-thread, value mask, online
+// Roles (320 threads):
+//   warps 0-7  softmax, two warpgroups splitting each row's columns:
+//              tcgen05.ld S (32x32b: one row per thread), value mask, online
 //              (m, l) update with lazy O rescale, P (bf16) back into TMEM
 //              over S's columns, epilogue O / l -> bf16 global stores.
-//   warp 4     TMA producer: Q once per unit, then K/V sub-tiles into a ring
+//   warp 8     TMA producer: Q once per unit, then K/V sub-tiles into a ring
 //              of 16 KB shared-memory slots.
-//   warp 5     TMEM allocation and the single MMA-issuing thread:
+//   warp 9     TMEM allocation and the single MMA-issuing thread:
 //              S = Q K^T (both operands in shared memory) and
 //              O += P V (P from TMEM, V from shared memory).
 //
@@ -59,6 +60,12 @@ struct PrefillParams {
 
 enum : int { kDebugDropArrive = 1 };
 
+// Warp roles: 0-7 softmax (two warpgroups), 8 TMA producer, 9 TMEM + MMA.
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kSoftmaxThreads = 256;
+
 // Sites recorded in the status word when a bounded wait expires.
 enum : int {
   kSiteQEmpty = 1, kSiteSlotEmpty, kSiteQFull, kSiteSlotFull, kSitePFull, kSiteSFull,
@@ -77,11 +84,14 @@ struct Layout {
   static constexpr int OFF_RING = Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + NSLOT * SUB;
   // barrier indices
+  // O_DONE b completes with every PV of a tile t with t % 2 == b.
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_SFULL = 2, B_PFULL = 4, B_ODONE = 6,
-                       B_DRAIN = 7, B_SLOTFULL = 8, B_SLOTEMPTY = 8 + NSLOT;
-  static constexpr int NBAR = 8 + 2 * NSLOT;
+                       B_DRAIN = 8, B_SLOTFULL = 9, B_SLOTEMPTY = 9 + NSLOT;
+  static constexpr int NBAR = 9 + 2 * NSLOT;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base
+  static constexpr int OFF_XCH = OFF_MISC + 16;           // [2][128] fp32 row exchange
+  static constexpr int OFF_PFAIL = OFF_XCH + 1024;         // [4] int: a pair member gave up
+  static constexpr int SMEM_BYTES = OFF_PFAIL + 16 + 1024;  // + slack to align the base
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_QK = make_idesc_bf16(kBQ, kBKV, false);
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(kBQ, HD, true);
@@ -245,7 +255,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
       mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
       rp.template advance<Ly::NSLOT>();
     }
-    mma_commit(bar(Ly::B_ODONE));
+    mma_commit(bar(Ly::B_ODONE + static_cast<int>(t & 1u)));
     return true;
   };
 
@@ -303,100 +313,123 @@ __device__ __forceinline__ uint32_t causal_word(int lim, int q) {
 }
 
 // ------------------------------------------------------- softmax + epilogue
+// Two warpgroups share the 128 rows: warp w (0..7) reads TMEM lanes
+// 32*(w%4).. (its rows) and owns half h = w/4 of every row's columns --
+// S columns [64h, 64h+64), O columns [h*HD/2, (h+1)*HD/2).  Warps w and w^4
+// hold the same rows; they agree on the row max through a paired barrier.
 template <int HD, bool SPLIT>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                              const BoundedWait& wait) {
   using Ly = Layout<HD>;
   auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
-  const int r = threadIdx.x;  // query row within the 128-row block == TMEM lane
+  const int warp = threadIdx.x >> 5;
+  const int h = warp >> 2;                              // column half
+  const int r = ((warp & 3) << 5) | (threadIdx.x & 31);  // row == TMEM lane
+  const uint32_t pair_bar = 1u + static_cast<uint32_t>(warp & 3);  // named barrier of the pair
   const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(r & ~31) << 16);
+  float* xch = reinterpret_cast<float*>(
+      __cvta_shared_to_generic(sbase + Ly::OFF_XCH));   // [2][128] exchange slots
+  // A warp whose bounded wait expired must not leave while its partner may
+  // still reach a pair barrier: it raises the pair's flag and keeps going to
+  // the next pair barrier, after which both read the flag and leave together.
+  volatile int* pair_fail = reinterpret_cast<volatile int*>(
+      __cvta_shared_to_generic(sbase + Ly::OFF_PFAIL)) + (warp & 3);
   const float sl2 = p.scale_log2;
   uint32_t tile_ctr = 0;
-  bool drop_one = (p.debug_flags & kDebugDropArrive) && blockIdx.x == 0 && r == 0;
+  bool drop_one = (p.debug_flags & kDebugDropArrive) && blockIdx.x == 0 && threadIdx.x == 0;
+  constexpr int OCOLS = HD / 2;                         // O columns of this half
 
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     const Unit U = decode_unit(p, u);
     CacheWalk walk;
     walk.init(U.L, p.P, p.S);
-    float m = -INFINITY;  // running max of the scaled logits, log2 units
-    float l = 0.f;        // running sum of 2^(x - m)
+    float m = -INFINITY;  // running reference max of the scaled logits (log2 units), per row
+    float l = 0.f;        // this half's running sum of 2^(x - m)
     bool ok = true;
+    bool left_at_vote = false;  // the only way out of the tile loop before its end
 
     for (int v = 0; v < U.n_tiles; ++v) {
       const uint32_t sb = tile_ctr & 1u;
       ok = wait(bar(Ly::B_SFULL + sb), (tile_ctr >> 1) & 1u, kSiteSFull);
       ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) break;
+      if (!ok) *pair_fail = 1;  // decided at the vote below, together with the partner
       tc_fence_after();
-      const uint32_t s_tmem = lane_tmem + HD + sb * kBKV;
+      const uint32_t s_tmem = lane_tmem + HD + sb * kBKV + 64 * h;
 
       // Region by value: one scalar picks the validity words of the tile.
       const bool in_cache = v < U.n_cache;
       uint32_t mw[4];
       if (in_cache) {
-        walk.column_mask(walk.next(), mw);
+        const int tile = walk.next();
+        if (walk.last_full) {
+          mw[0] = mw[1] = mw[2] = mw[3] = 0xFFFFFFFFu;
+        } else {
+          walk.column_mask(tile, mw);
+        }
       } else {
         const int lim = (v - U.n_cache == U.qb) ? r + 1 : kBKV;
 #pragma unroll
         for (int q = 0; q < 4; ++q) mw[q] = causal_word(lim, q);
       }
-      const bool need_mask =
-          __any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu);
+      const uint32_t w0 = h ? mw[2] : mw[0], w1 = h ? mw[3] : mw[1];
+      const bool need_mask = __any_sync(0xFFFFFFFFu, (w0 & w1) != 0xFFFFFFFFu);
 
-      // Pass 1: row max of the logits, streamed from TMEM 32 columns at a
-      // time (next chunk's load in flight).  On a partly masked tile the
-      // masked logits are written back as -inf, so pass 2 carries no mask.
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-      {
-        uint32_t ra[32], rb[32];
-        auto chunk_max = [&](uint32_t (&x)[32], uint32_t word, int q) {
-          if (need_mask) {
+      // Pass 1: load this half's 64 logits (two 32-column TMEM loads in
+      // flight together), mask by value, and take their max.  The registers
+      // stay live for pass 2.
+      uint32_t ra[32], rb[32];
+      tmem_ld32_async(s_tmem, ra);
+      tmem_ld32_async(s_tmem + 32, rb);
+      tmem_ld32_fence(ra);
+      tmem_ld32_fence(rb);
+      if (need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              x[i] = ((word >> i) & 1u) ? x[i] : 0xFF800000u;  // -inf
-            tmem_st32(s_tmem + 32 * q, x);
-          }
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            mx0 = fmaxf(mx0, __uint_as_float(x[i]));
-            mx1 = fmaxf(mx1, __uint_as_float(x[i + 1]));
-            mx2 = fmaxf(mx2, __uint_as_float(x[i + 2]));
-            mx3 = fmaxf(mx3, __uint_as_float(x[i + 3]));
-          }
-        };
-        tmem_ld32_async(s_tmem, ra);
-        tmem_ld32_fence(ra);
-        tmem_ld32_async(s_tmem + 32, rb);
-        chunk_max(ra, mw[0], 0);
-        tmem_ld32_fence(rb);
-        tmem_ld32_async(s_tmem + 64, ra);
-        chunk_max(rb, mw[1], 1);
-        tmem_ld32_fence(ra);
-        tmem_ld32_async(s_tmem + 96, rb);
-        chunk_max(ra, mw[2], 2);
-        tmem_ld32_fence(rb);
-        chunk_max(rb, mw[3], 3);
-        if (need_mask) tmem_wait_st();
+        for (int i = 0; i < 32; ++i) {
+          ra[i] = ((w0 >> i) & 1u) ? ra[i] : 0xFF800000u;  // -inf
+          rb[i] = ((w1 >> i) & 1u) ? rb[i] : 0xFF800000u;
+        }
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      const float m_new = fmaxf(m, m_tile);
-      // Lazy rescale: keep the old reference max unless the new one exceeds
-      // it by more than 2^8; the final O / l is the same either way.
-      const bool need = (v > 0) && (m_new > m + 8.f);
-      const bool warp_rescale = __any_sync(0xFFFFFFFFu, need);
-      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
-      if (v == 0 || need) m = m_new;
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        mx0 = fmaxf(mx0, __uint_as_float(ra[i]));
+        mx1 = fmaxf(mx1, __uint_as_float(ra[i + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(rb[i]));
+        mx3 = fmaxf(mx3, __uint_as_float(rb[i + 1]));
+      }
+      const float m_half = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
 
-      // Pass 2: p = 2^(x - m) and the row sum.  Chunk q (32 columns) holds,
-      // over its own 32 columns of the S buffer, P_hi = bf16(p) in the first
-      // 16 and -- accurate mode -- P_lo = bf16(p - P_hi) in the next 16.
+      // Lazy rescale: the reference max moves only when a row's new logits
+      // exceed it by more than 2^8 (the final O / l is the same either way).
+      // The pair votes; only then do the halves exchange their maxima.
+      float alpha = 1.f;
+      bool warp_rescale = false;
+      const bool any_need =
+          bar_red_or(pair_bar, 64, !ok || *pair_fail != 0 || v == 0 || m_half > m + 8.f);
+      if (any_need) {
+        if (*pair_fail) {  // read by both warps after the same barrier
+          left_at_vote = true;
+          break;
+        }
+        xch[h * 128 + r] = m_half;
+        bar_sync(pair_bar, 64);
+        const float m_tile = fmaxf(m_half, xch[(h ^ 1) * 128 + r]);
+        const float m_new = fmaxf(m, m_tile);
+        const bool need = (v > 0) && (m_new > m + 8.f);
+        alpha = need ? ex2_approx(m - m_new) : 1.f;
+        warp_rescale = __any_sync(0xFFFFFFFFu, need);
+        if (v == 0 || need) m = m_new;
+      }
+
+      // Pass 2: p = 2^(x - m) and this half's row sum.  Chunk q (32 keys)
+      // holds, over its own 32 columns of the S buffer, P_hi = bf16(p) in the
+      // first 16 and -- accurate mode -- P_lo = bf16(p - P_hi) in the next 16.
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       const float2 sl2x2 = make_float2(sl2, sl2);
       const float2 negm2 = make_float2(neg_m, neg_m);
       const float2 minus1 = make_float2(-1.f, -1.f);
       float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
       {
-        uint32_t ra[32], rb[32];
         auto chunk_exp = [&](const uint32_t (&x)[32], int q) {
           uint32_t hi[16], lo[16];
 #pragma unroll
@@ -417,38 +450,36 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
           tmem_st16(s_tmem + 32 * q, hi);
           if (SPLIT) tmem_st16(s_tmem + 32 * q + 16, lo);
         };
-        tmem_ld32_async(s_tmem, ra);
-#pragma unroll 1
-        for (int q = 0; q < 4; q += 2) {
-          tmem_ld32_fence(ra);
-          tmem_ld32_async(s_tmem + 32 * (q + 1), rb);
-          chunk_exp(ra, q);
-          tmem_ld32_fence(rb);
-          if (q + 2 < 4) tmem_ld32_async(s_tmem + 32 * (q + 2), ra);
-          chunk_exp(rb, q + 1);
-        }
+        chunk_exp(ra, 0);
+        chunk_exp(rb, 1);
       }
       l = l * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
-      // Observe the completion of PV of the previous tile (global index
-      // tile_ctr - 1) before releasing P of this one.  Every PV completion is
-      // observed in order: an mbarrier parity wait is unambiguous only while
-      // the waiter is at most one phase behind, and PV of this tile cannot
-      // start before this thread's arrival below.  The first tile of a unit
-      // skips it: the previous unit's epilogue observed that completion.
-      if (v > 0) {
-        ok = wait(bar(Ly::B_ODONE), (tile_ctr - 1) & 1u, kSiteODone);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) break;
+      // PV completions are observed in order, two tiles behind: PV of tile
+      // t-2 on barrier O_DONE[t % 2] (normally complete already: it ran before
+      // QK^T of tile t).  A parity wait is unambiguous only while the waiter is
+      // at most one phase behind; with the two barriers and PV of tile t held
+      // back by this thread's arrival below, that always holds.  Only a tile
+      // that rescales O also waits for PV of tile t-1.
+      auto pv_wait = [&](uint32_t t) {
+        return wait(bar(Ly::B_ODONE + static_cast<int>(t & 1u)), (t >> 1) & 1u, kSiteODone);
+      };
+      if (tile_ctr >= 2) {
+        ok = __all_sync(0xFFFFFFFFu, pv_wait(tile_ctr - 2));
+        if (!ok) *pair_fail = 1;  // acted on at the next pair barrier
+      }
+      if (ok && warp_rescale) {
+        ok = __all_sync(0xFFFFFFFFu, pv_wait(tile_ctr - 1));
+        if (!ok) *pair_fail = 1;
         tc_fence_after();
-        if (warp_rescale) {
+        if (ok) {
 #pragma unroll 1
-          for (int ch = 0; ch < HD / 32; ++ch) {
+          for (int ch = 0; ch < OCOLS / 32; ++ch) {
             uint32_t o[32];
-            tmem_ld32_wait(lane_tmem + 32 * ch, o);
+            tmem_ld32_wait(lane_tmem + h * OCOLS + 32 * ch, o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(lane_tmem + 32 * ch, o);
+            tmem_st32(lane_tmem + h * OCOLS + 32 * ch, o);
           }
         }
       }
@@ -461,22 +492,34 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       }
       ++tile_ctr;
     }
-    if (!ok) break;
+    if (left_at_vote) break;  // both warps of the pair left together
 
-    // Epilogue: O / l -> bf16, valid rows only.
-    ok = wait(bar(Ly::B_ODONE), (tile_ctr - 1) & 1u, kSiteODone);
+    // Epilogue: the pair adds its half sums (the first barrier keeps the
+    // partner's last read of the exchange slot ahead of this write, and
+    // settles a failure raised after the last vote); each half stores its O
+    // columns as bf16 (valid rows only).
+    bar_sync(pair_bar, 64);
+    if (*pair_fail) break;
+    xch[h * 128 + r] = l;
+    bar_sync(pair_bar, 64);
+    const float l_row = l + xch[(h ^ 1) * 128 + r];
+    const uint32_t t_last = tile_ctr - 1;  // its commit covers every earlier MMA too
+    ok = wait(bar(Ly::B_ODONE + static_cast<int>(t_last & 1u)), (t_last >> 1) & 1u, kSiteODone);
     ok = __all_sync(0xFFFFFFFFu, ok);
-    if (!ok) break;
+    if (!ok) {
+      *pair_fail = 1;  // no pair barrier remains in this unit; the next vote settles it
+      continue;
+    }
     tc_fence_after();
     const int row = U.q0 + r;
     const bool valid = row < U.c;
-    const float inv_l = 1.f / l;
+    const float inv_l = 1.f / l_row;
     const long long tok = static_cast<long long>(U.b) * p.C + row;
-    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * p.nq + U.h) * HD);
+    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * p.nq + U.h) * HD + h * OCOLS);
 #pragma unroll 1
-    for (int ch = 0; ch < HD / 32; ++ch) {
+    for (int ch = 0; ch < OCOLS / 32; ++ch) {
       uint32_t o[32];
-      tmem_ld32_wait(lane_tmem + 32 * ch, o);
+      tmem_ld32_wait(lane_tmem + h * OCOLS + 32 * ch, o);
       if (valid) {
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
@@ -489,14 +532,15 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
         }
       }
     }
-    if (valid && p.lse != nullptr) p.lse[tok * p.nq + U.h] = (m + __log2f(l)) * 0.69314718055994531f;
+    if (h == 0 && valid && p.lse != nullptr)
+      p.lse[tok * p.nq + U.h] = (m + __log2f(l_row)) * 0.69314718055994531f;
     tc_fence_before();
   }
 }
 
 // ------------------------------------------------------------------ kernel
 template <int HD, bool SPLIT>
-__global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -509,18 +553,19 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Ly::NBAR; ++i)
-      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? 128u : 1u);
+      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? kSoftmaxThreads : 1u);
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) reinterpret_cast<volatile int*>(smem + Ly::OFF_PFAIL)[i] = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k_new);
     prefetch_tmap(&p.tm_v_new);
     prefetch_tmap(&p.tm_k_cache);
     prefetch_tmap(&p.tm_v_cache);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), Ly::TMEM_COLS);
     tmem_relinquish();
   }
@@ -530,9 +575,9 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
   const uint32_t tmem = *tmem_holder;
   const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
 
-  if (warp < 4) {
+  if (warp < kProducerWarp) {
     softmax_role<HD, SPLIT>(p, sbase, tmem, wait);
-  } else if (warp == 4) {
+  } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<HD>(p, sbase, wait);
   } else {
     if (lane == 0) mma_role<HD, SPLIT>(p, sbase, tmem, wait);
@@ -540,7 +585,7 @@ __global__ void __launch_bounds__(192, 1) prefill_kernel(const __grid_constant__
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, Ly::TMEM_COLS);
   }

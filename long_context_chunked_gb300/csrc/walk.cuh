@@ -28,6 +28,8 @@ struct CacheWalk {
   int k;          // next tile index (flat rows [k*BKV, k*BKV + BKV))
   int k_last;     // last tile of shard s's range
   int prev_last;  // last tile emitted so far
+  long long lo, hi;  // filled flat rows of shard s: [s*S, s*S + n_s)
+  bool last_full;    // the tile returned by next() lies wholly inside [lo, hi)
 
   __host__ __device__ __forceinline__ void init(int L_, int P_, int S_) {
     L = L_;
@@ -46,13 +48,15 @@ struct CacheWalk {
         s = P;
         return;
       }
-      const long long lo = static_cast<long long>(s) * S;
-      int first = static_cast<int>(lo / kBKV);
-      const int last = static_cast<int>((lo + f - 1) / kBKV);
+      const long long a = static_cast<long long>(s) * S;
+      int first = static_cast<int>(a / kBKV);
+      const int last = static_cast<int>((a + f - 1) / kBKV);
       if (first <= prev_last) first = prev_last + 1;
       if (first <= last) {
         k = first;
         k_last = last;
+        lo = a;
+        hi = a + f;
         return;
       }
     }
@@ -60,9 +64,13 @@ struct CacheWalk {
 
   __host__ __device__ __forceinline__ bool done() const { return s >= P; }
 
-  // Emit the current tile index and advance.
+  // Emit the current tile index and advance.  Interior tiles of a shard's
+  // range are wholly valid (last_full); only the tiles at its edges need the
+  // column mask.
   __host__ __device__ __forceinline__ int next() {
     const int t = k;
+    const long long r0 = static_cast<long long>(t) * kBKV;
+    last_full = r0 >= lo && r0 + kBKV <= hi;
     prev_last = t;
     if (k < k_last)
       ++k;
