@@ -83,7 +83,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -266,6 +266,17 @@ def dist_setup():
     return world, rank, local
 
 
+def aggregate_max(value: float, device=None) -> float:
+    """Max of a per-rank timing over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, world, rank):
     """The CPU oracle as the reference arm: rank 0 only, bounded samples."""
     if rank != 0:
@@ -300,7 +311,7 @@ METRIC = "fused prefill attention TFLOP/s per chunk (write_kv + prefill) on 1 GB
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cpattn", choices=["cpattn", "reference"])
     ap.add_argument("--config", default="32k", choices=sorted(BY_NAME))
@@ -331,11 +342,8 @@ def main():
     with ClockSampler(local) as clk:
         step_ms, prefill_ms = time_steps(st, args.steps, args.warmup, flush)
     torch.cuda.synchronize()
-    total_ms = sum(step_ms)
+    total_ms = aggregate_max(sum(step_ms), device)
     if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
     e2e_ms, h2d, d2h = time_e2e(st, max(3, args.steps // 2), args.warmup)
 

@@ -11,6 +11,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libcpattn.so")
+# Race-detection build: MMA groups serialised (see CPATTN_SERIALIZE_MMA).
+LIB_SERIALIZED = os.path.join(PKG, "libcpattn_serialized.so")
 SOURCES = ["cpattn.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -22,19 +24,22 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA library cannot be built")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "cpattn.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, serialized: bool = False) -> str:
+    lib = LIB_SERIALIZED if serialized else LIB
+    if not force and not _stale(lib):
+        return lib
     cmd = [nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I" + INCLUDE, "-o", LIB + ".tmp"] + [os.path.join(CSRC, s) for s in SOURCES]
+           "-I" + INCLUDE, "-o", lib + ".tmp"] + [os.path.join(CSRC, s) for s in SOURCES]
+    if serialized:
+        cmd.insert(2, "-DCPATTN_SERIALIZE_MMA")
     if verbose:
         cmd.insert(2, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -42,9 +47,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError("nvcc failed:\n" + r.stdout + r.stderr)
     if verbose:
         sys.stderr.write(r.stderr)
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+    os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                serialized="--serialized" in sys.argv))

@@ -230,6 +230,20 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   RingPos rp;
   uint32_t tile_ctr = 0, units = 0;
   bool ok = true;
+#ifdef CPATTN_SERIALIZE_MMA
+  // Race-detection build: every MMA group completes before the MMA thread
+  // moves on, which stretches the MMA side of every producer/consumer pair.
+  // A correct protocol gives the same results bit for bit.
+  uint32_t ser_phase = 0;
+  auto serialize = [&]() {
+    mma_commit(bar(Ly::B_DRAIN));
+    mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+    ser_phase ^= 1u;
+  };
+#else
+  auto serialize = []() {};
+  const uint32_t ser_phase = 0;
+#endif
 
   // O (+)= P_w V_w, P_w from the S buffer of global tile t.
   auto issue_pv = [&](int w, uint32_t t) {
@@ -252,6 +266,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
         mma_ts(tmem, pa, bd, Ly::IDESC_PV, (w | j | kk) != 0);
         if (SPLIT) mma_ts(tmem, pa + 16, bd, Ly::IDESC_PV, 1u);
       }
+      serialize();
       mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
       rp.template advance<Ly::NSLOT>();
     }
@@ -282,6 +297,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
           const uint64_t bd = make_sdesc_sw128(kb + kk * 32, 16, 1024);
           mma_ss(s_tmem, ad, bd, Ly::IDESC_QK, (c | kk) != 0);
         }
+        serialize();
         mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
         rp.template advance<Ly::NSLOT>();
       }
@@ -298,7 +314,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   }
   // Every MMA issued must complete before TMEM is released.
   mma_commit(bar(Ly::B_DRAIN));
-  mbar_wait_drain(bar(Ly::B_DRAIN), 0u, kDrainLimitNs);
+  mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
 }
 }  // namespace cpattn
 
