@@ -32,6 +32,14 @@ def _stale(lib: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def build_all(force: bool = False) -> None:
+    """Both variants, compiled concurrently."""
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(2) as ex:
+        for f in [ex.submit(build, force, False, False), ex.submit(build, force, False, True)]:
+            f.result()
+
+
 def build(force: bool = False, verbose: bool = False, serialized: bool = False) -> str:
     lib = LIB_SERIALIZED if serialized else LIB
     if not force and not _stale(lib):

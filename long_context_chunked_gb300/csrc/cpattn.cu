@@ -24,7 +24,8 @@ struct cpattn_ctx {
   int device = -1;
   int num_sms = 0;
   int* d_status = nullptr;           // device status word (timeouts)
-  bool attr_set[2][2] = {{false, false}, {false, false}};  // [HD == 256][split P]
+  int grid_cap[2][2][2] = {};  // [HD == 256][split P][paired]: 0 until set up
+  bool pair_ctas = true;      // CPATTN_NO_PAIRING=1 turns the paired kernel off
   int debug_flags = 0;
   unsigned long long timeout_ns = 1000ull * 1000 * 1000;
   bool debug_sync = false;
@@ -113,19 +114,54 @@ cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* wha
   return CPATTN_OK;
 }
 
-template <int HD, bool SPLIT>
+template <int HD, bool SPLIT, bool MC>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
   using Ly = cpattn::Layout<HD>;
-  bool& attr = ctx->attr_set[HD == 256][SPLIT];
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(cpattn::prefill_kernel<HD, SPLIT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kernel = cpattn::prefill_kernel<HD, SPLIT, MC>;
+  int& grid_cap = ctx->grid_cap[HD == 256][SPLIT][MC];
+  if (grid_cap == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Ly::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(prefill)");
-    attr = true;
+    grid_cap = ctx->num_sms;
+    if (MC) {
+      // Persistent grid of co-resident CTA pairs.
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(2 * ctx->num_sms, 1, 1);
+      q.blockDim = dim3(cpattn::kThreads, 1, 1);
+      q.dynamicSmemBytes = Ly::SMEM_BYTES;
+      cudaLaunchAttribute a[1];
+      a[0].id = cudaLaunchAttributeClusterDimension;
+      a[0].val.clusterDim.x = 2;
+      a[0].val.clusterDim.y = 1;
+      a[0].val.clusterDim.z = 1;
+      q.attrs = a;
+      q.numAttrs = 1;
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &q);
+      if (e != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        return fail(ctx, CPATTN_E_CUDA, "no co-resident CTA pair for the paired prefill kernel");
+      }
+      grid_cap = std::min(2 * clusters, ctx->num_sms & ~1);
+    }
   }
-  const int grid = std::min(prm->num_units, ctx->num_sms);
-  cpattn::prefill_kernel<HD, SPLIT><<<grid, cpattn::kThreads, Ly::SMEM_BYTES, stream>>>(*prm);
+  int grid = std::min(prm->num_units, grid_cap);
+  if (MC) grid &= ~1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(cpattn::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Ly::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = MC ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *prm);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "prefill launch");
   return after_launch(ctx, stream, "prefill launch");
 }
 
@@ -164,6 +200,8 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   if (!(c.softmax_scale > 0.f)) ctx->cfg.softmax_scale = 1.0f / std::sqrt(static_cast<float>(c.head_dim));
   const char* dbg = std::getenv("CPATTN_DEBUG");
   ctx->debug_sync = dbg != nullptr && dbg[0] == '1';
+  const char* nopair = std::getenv("CPATTN_NO_PAIRING");
+  ctx->pair_ctas = !(nopair != nullptr && nopair[0] == '1');
   int dev = -1, ndev = 0;
   if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0 && cudaGetDevice(&dev) == cudaSuccess) {
     ctx->device = dev;
@@ -315,7 +353,9 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
             encode3d(&prm.tm_k_new, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV) &&
             encode3d(&prm.tm_v_new, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, vrows) &&
             encode3d(&prm.tm_k_cache, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV) &&
-            encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows);
+            encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows) &&
+            encode3d(&prm.tm_k_new_h, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV / 2) &&
+            encode3d(&prm.tm_k_cache_h, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV / 2);
   if (!ok) return fail(ctx, CPATTN_E_CUDA, "cuTensorMapEncodeTiled failed");
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
@@ -337,9 +377,18 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool split = c.fast_p == 0;
-  if (HD == 256)
-    return split ? launch_prefill<256, true>(ctx, &prm, st) : launch_prefill<256, false>(ctx, &prm, st);
-  return split ? launch_prefill<128, true>(ctx, &prm, st) : launch_prefill<128, false>(ctx, &prm, st);
+  // Pair CTAs on adjacent q heads of one kv head when the group size allows.
+  const bool mc = ctx->pair_ctas && (prm.group % 2 == 0);
+  if (HD == 256) {
+    if (mc) return split ? launch_prefill<256, true, true>(ctx, &prm, st)
+                         : launch_prefill<256, false, true>(ctx, &prm, st);
+    return split ? launch_prefill<256, true, false>(ctx, &prm, st)
+                 : launch_prefill<256, false, false>(ctx, &prm, st);
+  }
+  if (mc) return split ? launch_prefill<128, true, true>(ctx, &prm, st)
+                       : launch_prefill<128, false, true>(ctx, &prm, st);
+  return split ? launch_prefill<128, true, false>(ctx, &prm, st)
+               : launch_prefill<128, false, false>(ctx, &prm, st);
 }
 
 }  // extern "C"
@@ -387,16 +436,16 @@ cpattn_status noalloc_setup(NoAllocDevice** out) {
       return CPATTN_E_CUDA;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return CPATTN_E_CUDA;
-    if (cudaFuncSetAttribute(cpattn::prefill_kernel<128, true>,
+    if (cudaFuncSetAttribute(cpattn::prefill_kernel<128, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              cpattn::Layout<128>::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn::prefill_kernel<128, false>,
+        cudaFuncSetAttribute(cpattn::prefill_kernel<128, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              cpattn::Layout<128>::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn::prefill_kernel<256, true>,
+        cudaFuncSetAttribute(cpattn::prefill_kernel<256, true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              cpattn::Layout<256>::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn::prefill_kernel<256, false>,
+        cudaFuncSetAttribute(cpattn::prefill_kernel<256, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              cpattn::Layout<256>::SMEM_BYTES) != cudaSuccess)
       return CPATTN_E_CUDA;
@@ -516,12 +565,12 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   const int grid = std::min(prm.num_units, dev->num_sms);
   const bool split = c.fast_p == 0;
   if (HD == 256 && split)
-    cpattn::prefill_kernel<256, true><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<256, true, false><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
   else if (HD == 256)
-    cpattn::prefill_kernel<256, false><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<256, false, false><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
   else if (split)
-    cpattn::prefill_kernel<128, true><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<128, true, false><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
   else
-    cpattn::prefill_kernel<128, false><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
+    cpattn::prefill_kernel<128, false, false><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_E_CUDA;
 }

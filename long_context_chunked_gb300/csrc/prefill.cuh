@@ -48,6 +48,8 @@ struct PrefillParams {
   CUtensorMap tm_v_new;    // [T, NKV, HD]      box 64 x 1 x VROWS
   CUtensorMap tm_k_cache;  // [rows, 1, HD]     box 64 x 1 x 128
   CUtensorMap tm_v_cache;  // [rows, 1, HD]     box 64 x 1 x VROWS
+  CUtensorMap tm_k_new_h;    // as tm_k_new,   box 64 x 1 x 64 (half a tile, paired CTAs)
+  CUtensorMap tm_k_cache_h;  // as tm_k_cache, box 64 x 1 x 64
   __nv_bfloat16* out;
   float* lse;
   int* status;
@@ -141,7 +143,7 @@ namespace cpattn {
 constexpr unsigned long long kDrainLimitNs = 200ull * 1000 * 1000;
 
 // ------------------------------------------------------------- TMA producer
-template <int HD>
+template <int HD, bool MC>
 __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t sbase,
                                               const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -151,15 +153,37 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
   uint32_t q_issued = 0;
   bool ok = true;
 
-  // One 16 KB ring slot: wait until the MMA released it, then `nbox` boxes
-  // of 64 columns starting at column x0.
-  auto load_sub = [&](const CUtensorMap* m, int x0, int y, int z, int nbox, int box_bytes) {
+  // Paired CTAs (MC): both walk the same K/V tiles for two q heads of one kv
+  // head; each loads half of every sub-tile and multicasts it into the same
+  // slot of both CTAs, so every tile leaves L2 once per pair.  A slot is
+  // refilled only after both CTAs' MMAs released it (its empty barrier
+  // counts one multicast commit from each).
+  const int rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
+
+  // One 16 KB ring slot: wait until the slot is free, expect its 16 KB,
+  // then issue this CTA's boxes (`nbox` boxes of 64 columns from column x0;
+  // with MC the K half-tile rows or half of the V column boxes).
+  auto load_sub = [&](bool is_k, const CUtensorMap* m, const CUtensorMap* m_half, int x0, int y,
+                      int z) {
     if (rp.round && !wait(bar(Ly::B_SLOTEMPTY + rp.slot), rp.phase ^ 1u, kSiteSlotEmpty))
       return false;
     const uint32_t full = bar(Ly::B_SLOTFULL + rp.slot);
     mbar_arrive_expect_tx(full, Ly::SUB);
     const uint32_t dst = sbase + Ly::OFF_RING + static_cast<uint32_t>(rp.slot) * Ly::SUB;
-    for (int i = 0; i < nbox; ++i) tma_load_3d(dst + i * box_bytes, m, full, x0 + 64 * i, y, z);
+    if (is_k) {
+      if (MC)
+        tma_load_3d_mc(dst + rank * (Ly::SUB / 2), m_half, full, x0, y, z + rank * (kBKV / 2), 0x3);
+      else
+        tma_load_3d(dst, m, full, x0, y, z);
+    } else {
+      constexpr int BOX = Ly::VROWS * 128;
+      if (MC) {
+        for (int i = rank * (Ly::KCH / 2); i < (rank + 1) * (Ly::KCH / 2); ++i)
+          tma_load_3d_mc(dst + i * BOX, m, full, 64 * i, y, z, 0x3);
+      } else {
+        for (int i = 0; i < Ly::KCH; ++i) tma_load_3d(dst + i * BOX, m, full, 64 * i, y, z);
+      }
+    }
     rp.template advance<Ly::NSLOT>();
     ++issued;
     return true;
@@ -187,10 +211,11 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
       const bool in_cache = v < U.n_cache;
       const int tile = in_cache ? wk.next() : 0;
       const CUtensorMap* m = in_cache ? &p.tm_k_cache : &p.tm_k_new;
+      const CUtensorMap* mh = in_cache ? &p.tm_k_cache_h : &p.tm_k_new_h;
       const int y = in_cache ? 0 : U.g;
       const int z = in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV;
       for (int c = 0; c < Ly::KCH; ++c)
-        if (!load_sub(m, 64 * c, y, z, 1, 0)) return false;
+        if (!load_sub(true, m, mh, 64 * c, y, z)) return false;
       return true;
     };
     auto load_v = [&](int v) {
@@ -200,7 +225,7 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
       const int y = in_cache ? 0 : U.g;
       const int z = in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV;
       for (int j = 0; j < Ly::VSUB; ++j)
-        if (!load_sub(m, 0, y, z + j * Ly::VROWS, Ly::KCH, Ly::VROWS * 128)) return false;
+        if (!load_sub(false, m, m, 0, y, z + j * Ly::VROWS)) return false;
       return true;
     };
     // Same order as the MMA consumes them: K0, (K1, V0), (K2, V1), ..., V_last.
@@ -220,7 +245,7 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
 }
 
 // ------------------------------------------------------------- MMA issuer
-template <int HD, bool SPLIT>
+template <int HD, bool SPLIT, bool MC>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                          const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -230,6 +255,10 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   RingPos rp;
   uint32_t tile_ctr = 0, units = 0;
   bool ok = true;
+  // A slot is released to the producers of every CTA that shares it.
+  auto release_slot = [](uint32_t b) {
+    if (MC) mma_commit_mc(b, 0x3); else mma_commit(b);
+  };
 #ifdef CPATTN_SERIALIZE_MMA
   // Race-detection build: every MMA group completes before the MMA thread
   // moves on, which stretches the MMA side of every producer/consumer pair.
@@ -267,7 +296,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
         if (SPLIT) mma_ts(tmem, pa + 16, bd, Ly::IDESC_PV, 1u);
       }
       serialize();
-      mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
+      release_slot(bar(Ly::B_SLOTEMPTY + rp.slot));
       rp.template advance<Ly::NSLOT>();
     }
     mma_commit(bar(Ly::B_ODONE + static_cast<int>(t & 1u)));
@@ -298,7 +327,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
           mma_ss(s_tmem, ad, bd, Ly::IDESC_QK, (c | kk) != 0);
         }
         serialize();
-        mma_commit(bar(Ly::B_SLOTEMPTY + rp.slot));
+        release_slot(bar(Ly::B_SLOTEMPTY + rp.slot));
         rp.template advance<Ly::NSLOT>();
       }
       if (!ok) break;
@@ -555,7 +584,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 }
 
 // ------------------------------------------------------------------ kernel
-template <int HD, bool SPLIT>
+template <int HD, bool SPLIT, bool MC>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -569,7 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Ly::NBAR; ++i)
-      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? kSoftmaxThreads : 1u);
+      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? kSoftmaxThreads
+                        : (MC && i >= Ly::B_SLOTEMPTY)                ? 2u
+                                                                      : 1u);
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) reinterpret_cast<volatile int*>(smem + Ly::OFF_PFAIL)[i] = 0;
     fence_mbar_init();
@@ -580,13 +611,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     prefetch_tmap(&p.tm_v_new);
     prefetch_tmap(&p.tm_k_cache);
     prefetch_tmap(&p.tm_v_cache);
+    if (MC) {
+      prefetch_tmap(&p.tm_k_new_h);
+      prefetch_tmap(&p.tm_k_cache_h);
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), Ly::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // With MC the peer multicasts into this CTA's slots and barriers: no copy
+  // may start before both CTAs initialised their barriers.
+  if (MC) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
@@ -594,9 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (warp < kProducerWarp) {
     softmax_role<HD, SPLIT>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<HD>(p, sbase, wait);
+    if (lane == 0) producer_role<HD, MC>(p, sbase, wait);
   } else {
-    if (lane == 0) mma_role<HD, SPLIT>(p, sbase, tmem, wait);
+    if (lane == 0) mma_role<HD, SPLIT, MC>(p, sbase, tmem, wait);
   }
   __syncwarp();
   tc_fence_before();
@@ -605,6 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     tmem_dealloc(tmem, Ly::TMEM_COLS);
   }
+  // Neither CTA of a pair leaves while the other may still write into it.
+  if (MC) cluster_sync();
 }
 
 }  // namespace cpattn
