@@ -122,6 +122,27 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
                              void* out, float* lse, void* stream);
 
 /*
+ * The two-launch variant the PR removed (Summary section: a cache-only launch
+ * plus an LSE merge, strictly slower than the fused kernel), kept to measure
+ * what fusion saves: launch 1 attends every valid row to the cache only,
+ * launch 2 to its own chunk only (causal), each writing fp32 partial O and
+ * LSE into `workspace`; launch 3 merges them into bf16 `out` (and `lse`):
+ *   O = (e^{l1-m} O1 + e^{l2-m} O2) / (e^{l1-m} + e^{l2-m}),  m = max(l1, l2).
+ * Same arguments and result as cpattn_prefill, plus a caller-owned device
+ * workspace of at least cpattn_two_launch_workspace() bytes, 256-byte
+ * aligned, used only during the call's kernels on `stream`.
+ * Errors: as cpattn_prefill; E_INVALID also for a small or misaligned workspace.
+ */
+cpattn_status cpattn_two_launch_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
+                                          uint64_t* bytes);
+cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
+                                        const int32_t* cache_lens, const int32_t* chunk_lens,
+                                        const void* q, const void* k_new, const void* v_new,
+                                        const void* k_cache, const void* v_cache, void* out,
+                                        float* lse, void* workspace, uint64_t workspace_bytes,
+                                        void* stream);
+
+/*
  * Synchronise `stream`, then read and clear the context's device status word.
  * Returns E_TIMEOUT if a kernel launched with this context gave up on a
  * bounded wait since the last call (its outputs are then incomplete), E_CUDA

@@ -23,7 +23,8 @@ MAX_ROW_BLOCKS = 2048
 # Every symbol include/cpattn.h declares.
 EXPORTS = ("cpattn_create", "cpattn_write_kv", "cpattn_prefill", "cpattn_sync_status",
            "cpattn_set_fault_injection", "cpattn_cache_walk", "cpattn_destroy",
-           "cpattn_status_string", "cpattn_last_error", "cpattn_prefill_noalloc")
+           "cpattn_status_string", "cpattn_last_error", "cpattn_prefill_noalloc",
+           "cpattn_two_launch_workspace", "cpattn_prefill_two_launch")
 
 
 class CpattnError(RuntimeError):
@@ -73,6 +74,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cpattn_last_error.restype = ctypes.c_char_p
     lib.cpattn_prefill_noalloc.argtypes = [ctypes.POINTER(Config), I32, I32P, I32P] + [P] * 8
     lib.cpattn_prefill_noalloc.restype = I32
+    lib.cpattn_two_launch_workspace.argtypes = [P, I32, ctypes.POINTER(ctypes.c_uint64)]
+    lib.cpattn_two_launch_workspace.restype = I32
+    lib.cpattn_prefill_two_launch.argtypes = [P, I32, I32P, I32P] + [P] * 8 + [ctypes.c_uint64, P]
+    lib.cpattn_prefill_two_launch.restype = I32
     _lib = lib
     return lib
 
@@ -155,6 +160,22 @@ class Context:
         self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
         self._check(self.prefill_raw(cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
                                      out, lse, stream))
+
+    def two_launch_workspace(self, num_seqs: int) -> int:
+        n = ctypes.c_uint64()
+        self._check(self.lib.cpattn_two_launch_workspace(self._h, num_seqs, ctypes.byref(n)))
+        return n.value
+
+    def prefill_two_launch(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out,
+                           workspace, lse=None, stream=None):
+        """The removed two-launch variant (cache-only + current-only + LSE merge)."""
+        self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
+        cl, clp = _i32(cache_lens)
+        ch, chp = _i32(chunk_lens)
+        nbytes = workspace.numel() * workspace.element_size()
+        self._check(self.lib.cpattn_prefill_two_launch(
+            self._h, len(cl), clp, chp, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+            _ptr(v_cache), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, _stream(stream)))
 
     def sync_status(self, stream=None) -> int:
         """Synchronise and return the status code (E_TIMEOUT if a device wait expired)."""

@@ -18,6 +18,7 @@
 #include "prefill.cuh"
 #include "walk.cuh"
 #include "write_kv.cuh"
+#include "merge.cuh"
 
 struct cpattn_ctx {
   cpattn_config cfg;
@@ -163,6 +164,85 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *prm);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "prefill launch");
   return after_launch(ctx, stream, "prefill launch");
+}
+
+// Build the launch description of one prefill (all regions, or one region
+// for the two-launch variant) and launch it.  Arguments already validated.
+cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
+                             const int32_t* chunk_lens, const void* q, const void* k_new,
+                             const void* v_new, const void* k_cache, const void* v_cache,
+                             void* out, float* lse, void* stream, int region, int out_f32) {
+  const cpattn_config& c = ctx->cfg;
+
+  // Row blocks (b, q block), longest first: a unit's cost is its tile count.
+  // region 1 (cache only) has no work for a sequence with an empty cache.
+  struct Blk { int work, b, qb; };
+  std::vector<Blk> blks;
+  std::vector<int> ncache(num_seqs);
+  for (int b = 0; b < num_seqs; ++b) {
+    ncache[b] = cpattn::cache_tile_count(cache_lens[b], c.num_shards, c.shard_capacity);
+    if (region == 1 && ncache[b] == 0) continue;
+    const int nqb = (chunk_lens[b] + kBQ - 1) / kBQ;
+    for (int qb = 0; qb < nqb; ++qb) {
+      const int work = (region == 2 ? 0 : ncache[b]) + (region == 1 ? 0 : qb + 1);
+      blks.push_back({work, b, qb});
+    }
+  }
+  if (blks.size() > CPATTN_MAX_ROW_BLOCKS)
+    return fail(ctx, CPATTN_E_UNSUPPORTED, "more than CPATTN_MAX_ROW_BLOCKS row blocks");
+  if (blks.empty()) return CPATTN_OK;
+  if (ctx->d_status == nullptr) return fail(ctx, CPATTN_E_CUDA, "no CUDA device");
+  std::stable_sort(blks.begin(), blks.end(), [](const Blk& a, const Blk& b) { return a.work > b.work; });
+
+  static thread_local cpattn::PrefillParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
+  const uint64_t T = static_cast<uint64_t>(num_seqs) * c.chunk_size;
+  const uint64_t rows = static_cast<uint64_t>(num_seqs) * NKV * c.num_shards * c.shard_capacity;
+  const uint32_t vrows = 8192u / static_cast<uint32_t>(HD);
+  const uint64_t rb = static_cast<uint64_t>(HD) * 2;
+  bool ok = encode3d(&prm.tm_q, q, HD, NQ, T, rb, rb * NQ, 64, 1, kBQ) &&
+            encode3d(&prm.tm_k_new, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV) &&
+            encode3d(&prm.tm_v_new, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, vrows) &&
+            encode3d(&prm.tm_k_cache, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV) &&
+            encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows) &&
+            encode3d(&prm.tm_k_new_h, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV / 2) &&
+            encode3d(&prm.tm_k_cache_h, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV / 2);
+  if (!ok) return fail(ctx, CPATTN_E_CUDA, "cuTensorMapEncodeTiled failed");
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.region = region;
+  prm.out_f32 = out_f32;
+  prm.status = ctx->d_status;
+  prm.timeout_ns = ctx->timeout_ns;
+  prm.nq = NQ;
+  prm.nkv = NKV;
+  prm.group = NQ / NKV;
+  prm.P = c.num_shards;
+  prm.S = c.shard_capacity;
+  prm.C = c.chunk_size;
+  prm.debug_flags = ctx->debug_flags;
+  prm.scale_log2 = c.softmax_scale * 1.4426950408889634f;
+  for (int b = 0; b < num_seqs; ++b)
+    prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], ncache[b], 0};
+  for (size_t i = 0; i < blks.size(); ++i)
+    prm.blocks[i] = (static_cast<uint32_t>(blks[i].b) << 16) | static_cast<uint32_t>(blks[i].qb);
+  prm.num_units = static_cast<int>(blks.size()) * NQ;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool split = c.fast_p == 0;
+  // Pair CTAs on adjacent q heads of one kv head when the group size allows.
+  const bool mc = ctx->pair_ctas && (prm.group % 2 == 0);
+  if (HD == 256) {
+    if (mc) return split ? launch_prefill<256, true, true>(ctx, &prm, st)
+                         : launch_prefill<256, false, true>(ctx, &prm, st);
+    return split ? launch_prefill<256, true, false>(ctx, &prm, st)
+                 : launch_prefill<256, false, false>(ctx, &prm, st);
+  }
+  if (mc) return split ? launch_prefill<128, true, true>(ctx, &prm, st)
+                       : launch_prefill<128, false, true>(ctx, &prm, st);
+  return split ? launch_prefill<128, true, false>(ctx, &prm, st)
+               : launch_prefill<128, false, false>(ctx, &prm, st);
 }
 
 }  // namespace
@@ -325,70 +405,92 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)))
     return fail(ctx, CPATTN_E_INVALID, "device pointers must be 16-byte aligned");
-  const cpattn_config& c = ctx->cfg;
+  return prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
+                        out, lse, stream, 0, 0);
+}
 
-  // Row blocks (b, q block), longest first: a unit's cost is its tile count.
-  struct Blk { int work, b, qb; };
-  std::vector<Blk> blks;
-  std::vector<int> ncache(num_seqs);
-  for (int b = 0; b < num_seqs; ++b) {
-    ncache[b] = cpattn::cache_tile_count(cache_lens[b], c.num_shards, c.shard_capacity);
-    const int nqb = (chunk_lens[b] + kBQ - 1) / kBQ;
-    for (int qb = 0; qb < nqb; ++qb) blks.push_back({ncache[b] + qb + 1, b, qb});
-  }
-  if (blks.size() > CPATTN_MAX_ROW_BLOCKS)
-    return fail(ctx, CPATTN_E_UNSUPPORTED, "more than CPATTN_MAX_ROW_BLOCKS row blocks");
-  if (blks.empty()) return CPATTN_OK;
-  if (ctx->d_status == nullptr) return fail(ctx, CPATTN_E_CUDA, "no CUDA device");
-  std::stable_sort(blks.begin(), blks.end(), [](const Blk& a, const Blk& b) { return a.work > b.work; });
+// Two-launch variant: workspace = two fp32 partial outputs and two LSE rows.
+static uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
-  static thread_local cpattn::PrefillParams prm;
-  std::memset(&prm, 0, sizeof(prm));
-  const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
+static void two_launch_layout(const cpattn_config& c, int32_t num_seqs, uint64_t off[4],
+                              uint64_t* total) {
   const uint64_t T = static_cast<uint64_t>(num_seqs) * c.chunk_size;
-  const uint64_t rows = static_cast<uint64_t>(num_seqs) * NKV * c.num_shards * c.shard_capacity;
-  const uint32_t vrows = 8192u / static_cast<uint32_t>(HD);
-  const uint64_t rb = static_cast<uint64_t>(HD) * 2;
-  bool ok = encode3d(&prm.tm_q, q, HD, NQ, T, rb, rb * NQ, 64, 1, kBQ) &&
-            encode3d(&prm.tm_k_new, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV) &&
-            encode3d(&prm.tm_v_new, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, vrows) &&
-            encode3d(&prm.tm_k_cache, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV) &&
-            encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows) &&
-            encode3d(&prm.tm_k_new_h, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV / 2) &&
-            encode3d(&prm.tm_k_cache_h, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV / 2);
-  if (!ok) return fail(ctx, CPATTN_E_CUDA, "cuTensorMapEncodeTiled failed");
-  prm.out = static_cast<__nv_bfloat16*>(out);
-  prm.lse = lse;
-  prm.status = ctx->d_status;
-  prm.timeout_ns = ctx->timeout_ns;
-  prm.nq = NQ;
-  prm.nkv = NKV;
-  prm.group = NQ / NKV;
-  prm.P = c.num_shards;
-  prm.S = c.shard_capacity;
-  prm.C = c.chunk_size;
-  prm.debug_flags = ctx->debug_flags;
-  prm.scale_log2 = c.softmax_scale * 1.4426950408889634f;
-  for (int b = 0; b < num_seqs; ++b)
-    prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], ncache[b], 0};
-  for (size_t i = 0; i < blks.size(); ++i)
-    prm.blocks[i] = (static_cast<uint32_t>(blks[i].b) << 16) | static_cast<uint32_t>(blks[i].qb);
-  prm.num_units = static_cast<int>(blks.size()) * NQ;
+  const uint64_t o = align256(T * c.num_q_heads * c.head_dim * sizeof(float));
+  const uint64_t l = align256(T * c.num_q_heads * sizeof(float));
+  off[0] = 0;
+  off[1] = o;
+  off[2] = 2 * o;
+  off[3] = 2 * o + l;
+  *total = 2 * o + 2 * l;
+}
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool split = c.fast_p == 0;
-  // Pair CTAs on adjacent q heads of one kv head when the group size allows.
-  const bool mc = ctx->pair_ctas && (prm.group % 2 == 0);
-  if (HD == 256) {
-    if (mc) return split ? launch_prefill<256, true, true>(ctx, &prm, st)
-                         : launch_prefill<256, false, true>(ctx, &prm, st);
-    return split ? launch_prefill<256, true, false>(ctx, &prm, st)
-                 : launch_prefill<256, false, false>(ctx, &prm, st);
+cpattn_status cpattn_two_launch_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
+                                          uint64_t* bytes) {
+  if (ctx == nullptr || bytes == nullptr || num_seqs < 1) return CPATTN_E_INVALID;
+  uint64_t off[4];
+  two_launch_layout(ctx->cfg, num_seqs, off, bytes);
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
+                                        const int32_t* cache_lens, const int32_t* chunk_lens,
+                                        const void* q, const void* k_new, const void* v_new,
+                                        const void* k_cache, const void* v_cache, void* out,
+                                        float* lse, void* workspace, uint64_t workspace_bytes,
+                                        void* stream) {
+  if (ctx == nullptr) return CPATTN_E_INVALID;
+  cpattn_status s = check_seqs(ctx, num_seqs, cache_lens, chunk_lens);
+  if (s != CPATTN_OK) return s;
+  if (q == nullptr || k_new == nullptr || v_new == nullptr || k_cache == nullptr ||
+      v_cache == nullptr || out == nullptr || workspace == nullptr)
+    return fail(ctx, CPATTN_E_INVALID, "device pointers must not be NULL");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(ctx, CPATTN_E_INVALID, "pointer alignment (16 B; workspace 256 B)");
+  const cpattn_config& c = ctx->cfg;
+  uint64_t off[4], need;
+  two_launch_layout(c, num_seqs, off, &need);
+  if (workspace_bytes < need)
+    return fail(ctx, CPATTN_E_INVALID,
+                "workspace too small: need " + std::to_string(need) + " bytes");
+  char* ws = static_cast<char*>(workspace);
+  float* o1 = reinterpret_cast<float*>(ws + off[0]);
+  float* o2 = reinterpret_cast<float*>(ws + off[1]);
+  float* l1 = reinterpret_cast<float*>(ws + off[2]);
+  float* l2 = reinterpret_cast<float*>(ws + off[3]);
+  // Launch 1: cache tiles only; launch 2: current tiles only (causal).
+  s = prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
+                     o1, l1, stream, 1, 1);
+  if (s != CPATTN_OK) return s;
+  s = prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
+                     o2, l2, stream, 2, 1);
+  if (s != CPATTN_OK) return s;
+  // Launch 3: LSE merge into bf16 O.
+  cpattn::MergeParams m;
+  m.o1 = o1;
+  m.lse1 = l1;
+  m.o2 = o2;
+  m.lse2 = l2;
+  m.out = static_cast<__nv_bfloat16*>(out);
+  m.lse = lse;
+  m.num_seqs = num_seqs;
+  m.C = c.chunk_size;
+  m.nq = c.num_q_heads;
+  m.hd = c.head_dim;
+  long long acc = 0;
+  for (int b = 0; b < num_seqs; ++b) {
+    m.has_cache[b] = cache_lens[b] > 0 ? 1 : 0;
+    m.item_prefix[b] = acc;
+    acc += static_cast<long long>(chunk_lens[b]) * c.num_q_heads * (c.head_dim / 8);
   }
-  if (mc) return split ? launch_prefill<128, true, true>(ctx, &prm, st)
-                       : launch_prefill<128, false, true>(ctx, &prm, st);
-  return split ? launch_prefill<128, true, false>(ctx, &prm, st)
-               : launch_prefill<128, false, false>(ctx, &prm, st);
+  m.item_prefix[num_seqs] = acc;
+  m.total = acc;
+  if (acc == 0) return CPATTN_OK;
+  const long long blocks = (acc + 255) / 256;
+  const int grid = static_cast<int>(std::min<long long>(blocks, static_cast<long long>(ctx->num_sms) * 16));
+  cpattn::lse_merge_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(m);
+  return after_launch(ctx, static_cast<cudaStream_t>(stream), "merge launch");
 }
 
 }  // extern "C"

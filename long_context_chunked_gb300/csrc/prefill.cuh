@@ -55,6 +55,10 @@ struct PrefillParams {
   int* status;
   unsigned long long timeout_ns;
   int num_units, nq, nkv, group, P, S, C, debug_flags;
+  // Region restriction (the two-launch variant): 0 both regions in one
+  // softmax, 1 cache tiles only, 2 current tiles only.  out_f32: O is written
+  // as fp32 (partial results for the LSE merge) instead of bf16.
+  int region, out_f32;
   float scale_log2;
   SeqInfo seqs[CPATTN_MAX_SEQS];
   uint32_t blocks[CPATTN_MAX_ROW_BLOCKS];  // (b << 16) | q block, longest first
@@ -116,8 +120,8 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
   U.q0 = U.qb * kBQ;
   U.L = p.seqs[U.b].cache_len;
   U.c = p.seqs[U.b].chunk_len;
-  U.n_cache = p.seqs[U.b].n_cache_tiles;
-  U.n_tiles = U.n_cache + U.qb + 1;
+  U.n_cache = p.region == 2 ? 0 : p.seqs[U.b].n_cache_tiles;
+  U.n_tiles = U.n_cache + (p.region == 1 ? 0 : U.qb + 1);
   return U;
 }
 
@@ -561,11 +565,19 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
     const float inv_l = 1.f / l_row;
     const long long tok = static_cast<long long>(U.b) * p.C + row;
     uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * p.nq + U.h) * HD + h * OCOLS);
+    float4* orow32 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
+                                               (tok * p.nq + U.h) * HD + h * OCOLS);
 #pragma unroll 1
     for (int ch = 0; ch < OCOLS / 32; ++ch) {
       uint32_t o[32];
       tmem_ld32_wait(lane_tmem + h * OCOLS + 32 * ch, o);
-      if (valid) {
+      if (valid && p.out_f32) {
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4)
+          orow32[ch * 8 + v4] = make_float4(
+              __uint_as_float(o[4 * v4]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
+              __uint_as_float(o[4 * v4 + 2]) * inv_l, __uint_as_float(o[4 * v4 + 3]) * inv_l);
+      } else if (valid) {
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
           uint4 pk;
