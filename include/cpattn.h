@@ -76,8 +76,14 @@ typedef struct cpattn_ctx cpattn_ctx; /* opaque */
  * Allocates a few bytes of device memory for the timeout status word on the
  * current device (skipped, without error, when no device is present; launches
  * then fail with CPATTN_E_CUDA).
- * Errors: E_INVALID (NULL, NQ % NKV != 0, sizes < 1), E_UNSUPPORTED (HD not
- * 128/256), E_NOMEM.
+ * The environment variable CPATTN_PAIRING, read here, picks how prefill
+ * pairs the CTAs of adjacent q heads of one kv head when NQ/NKV is even:
+ * "mma2" (default: the pair runs 2-SM tensor-core MMAs and each SM stages
+ * half of every K/V tile), "multicast" (each CTA runs its own MMAs, the pair
+ * shares K/V loads), "none" (one CTA per unit).  Results meet the same
+ * accuracy in every mode; the bits may differ between modes.
+ * Errors: E_INVALID (NULL, NQ % NKV != 0, sizes < 1, an unknown
+ * CPATTN_PAIRING), E_UNSUPPORTED (HD not 128/256), E_NOMEM.
  */
 cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out);
 

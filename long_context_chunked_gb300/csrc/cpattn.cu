@@ -16,6 +16,7 @@
 
 #include "cpattn.h"
 #include "prefill.cuh"
+#include "prefill_pair.cuh"
 #include "walk.cuh"
 #include "write_kv.cuh"
 #include "merge.cuh"
@@ -25,8 +26,10 @@ struct cpattn_ctx {
   int device = -1;
   int num_sms = 0;
   int* d_status = nullptr;           // device status word (timeouts)
-  int grid_cap[2][2][2] = {};  // [HD == 256][split P][paired]: 0 until set up
-  bool pair_ctas = true;      // CPATTN_NO_PAIRING=1 turns the paired kernel off
+  int grid_cap[2][2][3] = {};  // [HD == 256][split P][pairing mode]: 0 until set up
+  // CTA pairing for even group sizes (CPATTN_PAIRING = mma2 | multicast | none):
+  // 2 = 2-SM MMA pairs, 1 = pairs sharing K/V loads by multicast, 0 = off.
+  int pair_mode = 2;
   int debug_flags = 0;
   unsigned long long timeout_ns = 1000ull * 1000 * 1000;
   bool debug_sync = false;
@@ -115,11 +118,14 @@ cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* wha
   return CPATTN_OK;
 }
 
-template <int HD, bool SPLIT, bool MC>
+template <int HD, bool SPLIT, int MODE>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
   using Ly = cpattn::Layout<HD>;
-  auto kernel = cpattn::prefill_kernel<HD, SPLIT, MC>;
-  int& grid_cap = ctx->grid_cap[HD == 256][SPLIT][MC];
+  constexpr bool MC = MODE != 0;  // launched as clusters of two CTAs
+  void (*kernel)(cpattn::PrefillParams) = MODE == 2
+                                              ? cpattn::prefill_kernel_pair2<HD, SPLIT>
+                                              : cpattn::prefill_kernel<HD, SPLIT, MODE == 1>;
+  int& grid_cap = ctx->grid_cap[HD == 256][SPLIT][MODE];
   if (grid_cap == 0) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Ly::SMEM_BYTES);
@@ -207,7 +213,9 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
             encode3d(&prm.tm_k_cache, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV) &&
             encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows) &&
             encode3d(&prm.tm_k_new_h, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV / 2) &&
-            encode3d(&prm.tm_k_cache_h, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV / 2);
+            encode3d(&prm.tm_k_cache_h, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV / 2) &&
+            encode3d(&prm.tm_v_new_h, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, 64) &&
+            encode3d(&prm.tm_v_cache_h, v_cache, HD, 1, rows, rb, rb, 64, 1, 64);
   if (!ok) return fail(ctx, CPATTN_E_CUDA, "cuTensorMapEncodeTiled failed");
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
@@ -232,17 +240,21 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool split = c.fast_p == 0;
   // Pair CTAs on adjacent q heads of one kv head when the group size allows.
-  const bool mc = ctx->pair_ctas && (prm.group % 2 == 0);
+  const int mode = (prm.group % 2 == 0) ? ctx->pair_mode : 0;
   if (HD == 256) {
-    if (mc) return split ? launch_prefill<256, true, true>(ctx, &prm, st)
-                         : launch_prefill<256, false, true>(ctx, &prm, st);
-    return split ? launch_prefill<256, true, false>(ctx, &prm, st)
-                 : launch_prefill<256, false, false>(ctx, &prm, st);
+    if (mode == 2) return split ? launch_prefill<256, true, 2>(ctx, &prm, st)
+                                : launch_prefill<256, false, 2>(ctx, &prm, st);
+    if (mode == 1) return split ? launch_prefill<256, true, 1>(ctx, &prm, st)
+                                : launch_prefill<256, false, 1>(ctx, &prm, st);
+    return split ? launch_prefill<256, true, 0>(ctx, &prm, st)
+                 : launch_prefill<256, false, 0>(ctx, &prm, st);
   }
-  if (mc) return split ? launch_prefill<128, true, true>(ctx, &prm, st)
-                       : launch_prefill<128, false, true>(ctx, &prm, st);
-  return split ? launch_prefill<128, true, false>(ctx, &prm, st)
-               : launch_prefill<128, false, false>(ctx, &prm, st);
+  if (mode == 2) return split ? launch_prefill<128, true, 2>(ctx, &prm, st)
+                              : launch_prefill<128, false, 2>(ctx, &prm, st);
+  if (mode == 1) return split ? launch_prefill<128, true, 1>(ctx, &prm, st)
+                              : launch_prefill<128, false, 1>(ctx, &prm, st);
+  return split ? launch_prefill<128, true, 0>(ctx, &prm, st)
+               : launch_prefill<128, false, 0>(ctx, &prm, st);
 }
 
 }  // namespace
@@ -280,8 +292,16 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   if (!(c.softmax_scale > 0.f)) ctx->cfg.softmax_scale = 1.0f / std::sqrt(static_cast<float>(c.head_dim));
   const char* dbg = std::getenv("CPATTN_DEBUG");
   ctx->debug_sync = dbg != nullptr && dbg[0] == '1';
-  const char* nopair = std::getenv("CPATTN_NO_PAIRING");
-  ctx->pair_ctas = !(nopair != nullptr && nopair[0] == '1');
+  const char* pairing = std::getenv("CPATTN_PAIRING");
+  if (pairing != nullptr) {
+    if (std::strcmp(pairing, "none") == 0) ctx->pair_mode = 0;
+    else if (std::strcmp(pairing, "multicast") == 0) ctx->pair_mode = 1;
+    else if (std::strcmp(pairing, "mma2") == 0) ctx->pair_mode = 2;
+    else {
+      delete ctx;
+      return CPATTN_E_INVALID;
+    }
+  }
   int dev = -1, ndev = 0;
   if (cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0 && cudaGetDevice(&dev) == cudaSuccess) {
     ctx->device = dev;

@@ -50,6 +50,8 @@ struct PrefillParams {
   CUtensorMap tm_v_cache;  // [rows, 1, HD]     box 64 x 1 x VROWS
   CUtensorMap tm_k_new_h;    // as tm_k_new,   box 64 x 1 x 64 (half a tile, paired CTAs)
   CUtensorMap tm_k_cache_h;  // as tm_k_cache, box 64 x 1 x 64
+  CUtensorMap tm_v_new_h;    // as tm_v_new,   box 64 x 1 x 64 (2-SM MMA pairs)
+  CUtensorMap tm_v_cache_h;  // as tm_v_cache, box 64 x 1 x 64
   __nv_bfloat16* out;
   float* lse;
   int* status;
@@ -366,7 +368,10 @@ __device__ __forceinline__ uint32_t causal_word(int lim, int q) {
 // 32*(w%4).. (its rows) and owns half h = w/4 of every row's columns --
 // S columns [64h, 64h+64), O columns [h*HD/2, (h+1)*HD/2).  Warps w and w^4
 // hold the same rows; they agree on the row max through a paired barrier.
-template <int HD, bool SPLIT>
+// PAIR2: the CTA is one of a pair whose leader issues 2-SM MMAs; S, P and O
+// of this CTA's 128 rows sit in its own TMEM exactly as in a single CTA, but
+// "P ready" goes to the leader's barrier, one arrival per warp.
+template <int HD, bool SPLIT, bool PAIR2 = false>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                              const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -534,7 +539,15 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       }
       tmem_wait_st();
       tc_fence_before();
-      if (drop_one) {
+      if (PAIR2) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+          if (drop_one)
+            drop_one = false;  // fault-injection hook: this arrival never happens
+          else
+            mbar_arrive_remote(mapa_shared(bar(Ly::B_PFULL + sb), 0));
+        }
+      } else if (drop_one) {
         drop_one = false;  // fault-injection hook: this arrival never happens
       } else {
         mbar_arrive(bar(Ly::B_PFULL + sb));

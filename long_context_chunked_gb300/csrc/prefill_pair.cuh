@@ -1,0 +1,323 @@
+// The fused chunked-prefill kernel on PAIRS of SMs with 2-SM MMAs
+// (tcgen05 cta_group::2): the same single-pass algorithm as prefill.cuh (one
+// query chunk against its cached prefix and its own causal chunk, one online
+// softmax -- PCP ring-cache PR, Summary and Design sections), with the two
+// CTAs of a cluster working on two adjacent q heads of ONE kv head, i.e. on
+// the same K/V tiles.
+//
+// The leader CTA (cluster rank 0) issues every MMA for both:
+//   S[256 x 128]  = Q[256 x HD] K^T   rows 0-127: the leader's head, 128-255:
+//                                     the peer's; each CTA holds its own Q and
+//                                     64 of the tile's 128 keys (B split by N)
+//   O[256 x HD]  += P[256 x 128] V    P from each CTA's own TMEM; each CTA
+//                                     holds HD/2 of V's columns (B split by N)
+// so each SM stages HALF of every K and V tile (64 KB at HD = 256 instead of
+// 128 KB) and the same 16 KB-slot ring holds twice as many tiles.  TMEM use,
+// the softmax and the epilogue are those of the single-CTA kernel, per CTA.
+//
+// Ring slot contents (16 KB, 128-byte swizzle, boxes of 64 columns x 64 rows):
+//   K slot j:  chunks 2j, 2j+1 of this CTA's 64 key rows   (HD/128 slots)
+//   V slot j:  key rows [j*VR, j*VR + VR) x this CTA's HD/2 columns, one box
+//              per 64-column chunk (VR = 16384/HD rows)      (HD/128 slots)
+//
+// Barriers (per CTA; the leader's are the ones waited on):
+//   Q_FULL, SLOT_FULL  on the leader, count 2: one expect_tx arrival from each
+//                      CTA's producer; the bytes of both CTAs' copies complete
+//                      on them (cta_group::2 TMA)
+//   P_FULL             on the leader, count 16: one arrival per softmax warp
+//                      of both CTAs
+//   S_FULL, O_DONE, SLOT_EMPTY, Q_EMPTY   in both CTAs, count 1: multicast
+//                      commits of the leader's MMA thread
+#pragma once
+
+#include "prefill.cuh"
+
+namespace cpattn {
+
+template <int HD>
+struct PairLayout {
+  static constexpr int KSLOTS = HD / 128;      // K half-tile slots per tile
+  static constexpr int VSLOTS = HD / 128;      // V half-tile slots per tile
+  static constexpr int NH = HD / 2;            // V columns held by one CTA
+  static constexpr int VR = 16384 / HD;        // key rows per V slot
+  static constexpr int VCH = NH / 64;          // 64-column boxes per V slot row group
+  static constexpr int VRG = VR / 64;          // 64-row boxes per V slot column chunk
+  static constexpr int BOX = 8192;             // bytes per 64 x 64 box
+  static constexpr uint32_t IDESC_QK = make_idesc_bf16(2 * kBQ, kBKV, false);
+  static constexpr uint32_t IDESC_PV = make_idesc_bf16(2 * kBQ, HD, true);
+  static constexpr uint32_t P_ARRIVALS = 2 * kSoftmaxThreads / 32;
+  static_assert(VCH * VRG * BOX == Layout<HD>::SUB, "V slot = 16 KB");
+  static_assert(2 * BOX == Layout<HD>::SUB, "K slot = two chunks of 64 rows");
+};
+
+// ------------------------------------------------------------- TMA producer
+// Both CTAs: this CTA's half of every K and V tile, and its own Q, each copy
+// completing on the leader's barrier.
+template <int HD>
+__device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint32_t sbase,
+                                                    const BoundedWait& wait) {
+  using Ly = Layout<HD>;
+  using Pl = PairLayout<HD>;
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  const uint32_t rank = cluster_ctarank();
+  auto lead = [&](int i) { return mapa_shared(bar(i), 0); };
+  RingPos rp;
+  long long issued = 0;
+  uint32_t q_issued = 0;
+  bool ok = true;
+
+  // One slot: wait until both CTAs' last use of it completed (the leader's
+  // MMAs released it), announce 16 KB on the leader's full barrier, then
+  // issue this CTA's boxes (emit(dst) issues them).
+  auto load_slot = [&](auto&& emit) {
+    if (rp.round && !wait(bar(Ly::B_SLOTEMPTY + rp.slot), rp.phase ^ 1u, kSiteSlotEmpty))
+      return false;
+    const uint32_t full = lead(Ly::B_SLOTFULL + rp.slot);
+    mbar_arrive_expect_tx_remote(full, Ly::SUB);
+    emit(sbase + Ly::OFF_RING + static_cast<uint32_t>(rp.slot) * Ly::SUB, full);
+    rp.template advance<Ly::NSLOT>();
+    ++issued;
+    return true;
+  };
+
+  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+    const Unit U = decode_unit(p, u);
+    if (q_issued > 0 && !wait(bar(Ly::B_QEMPTY), (q_issued - 1) & 1u, kSiteQEmpty)) {
+      ok = false;
+      break;
+    }
+    const uint32_t qfull = lead(Ly::B_QFULL);
+    mbar_arrive_expect_tx_remote(qfull, Ly::Q_BYTES);
+    for (int c = 0; c < Ly::KCH; ++c)
+      tma_load_3d_pair(sbase + Ly::OFF_Q + c * (kBQ * 128), &p.tm_q, qfull, 64 * c, U.h,
+                       U.b * p.C + U.q0);
+    ++q_issued;
+
+    const int head_row = ((U.b * p.nkv + U.g) * p.P) * p.S;
+    CacheWalk wk, wv;
+    wk.init(U.L, p.P, p.S);
+    wv.init(U.L, p.P, p.S);
+    // Tile v's source is chosen by value, as in the single-CTA producer.
+    auto load_k = [&](int v) {
+      const bool in_cache = v < U.n_cache;
+      const int tile = in_cache ? wk.next() : 0;
+      const CUtensorMap* m = in_cache ? &p.tm_k_cache_h : &p.tm_k_new_h;
+      const int y = in_cache ? 0 : U.g;
+      const int z = (in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV) +
+                    static_cast<int>(rank) * (kBKV / 2);
+      for (int j = 0; j < Pl::KSLOTS; ++j) {
+        const bool r = load_slot([&](uint32_t dst, uint32_t full) {
+          tma_load_3d_pair(dst, m, full, 64 * (2 * j), y, z);
+          tma_load_3d_pair(dst + Pl::BOX, m, full, 64 * (2 * j + 1), y, z);
+        });
+        if (!r) return false;
+      }
+      return true;
+    };
+    auto load_v = [&](int v) {
+      const bool in_cache = v < U.n_cache;
+      const int tile = in_cache ? wv.next() : 0;
+      const CUtensorMap* m = in_cache ? &p.tm_v_cache_h : &p.tm_v_new_h;
+      const int y = in_cache ? 0 : U.g;
+      const int z = in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV;
+      const int x0 = static_cast<int>(rank) * Pl::NH;
+      for (int j = 0; j < Pl::VSLOTS; ++j) {
+        const bool r = load_slot([&](uint32_t dst, uint32_t full) {
+          for (int i = 0; i < Pl::VCH; ++i)
+            for (int g = 0; g < Pl::VRG; ++g)
+              tma_load_3d_pair(dst + (i * Pl::VRG + g) * Pl::BOX, m, full, x0 + 64 * i, y,
+                               z + j * Pl::VR + 64 * g);
+        });
+        if (!r) return false;
+      }
+      return true;
+    };
+    // Same order as the MMA consumes them: K0, (K1, V0), (K2, V1), ..., V_last.
+    ok = load_k(0);
+    for (int v = 1; ok && v < U.n_tiles; ++v) ok = load_k(v) && load_v(v - 1);
+    if (ok) ok = load_v(U.n_tiles - 1);
+  }
+
+  if (!ok && rank == 0) {
+    // The leader's full barriers count both CTAs' copies: let every phase
+    // the leader took part in land before the pair can leave (bounded; a
+    // phase the peer never joined gives up after the drain limit).
+    const long long first = issued > Ly::NSLOT ? issued - Ly::NSLOT : 0;
+    for (long long z = first; z < issued; ++z)
+      mbar_wait_drain(bar(Ly::B_SLOTFULL + static_cast<int>(z % Ly::NSLOT)),
+                      static_cast<uint32_t>((z / Ly::NSLOT) & 1), kDrainLimitNs);
+    if (q_issued > 0) mbar_wait_drain(bar(Ly::B_QFULL), (q_issued - 1) & 1u, kDrainLimitNs);
+  }
+}
+
+// ------------------------------------------------------------- MMA issuer
+// Leader CTA only, one thread.
+template <int HD, bool SPLIT>
+__device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t sbase,
+                                               uint32_t tmem, const BoundedWait& wait) {
+  using Ly = Layout<HD>;
+  using Pl = PairLayout<HD>;
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  const uint32_t q_base = sbase + Ly::OFF_Q;
+  const uint32_t ring = sbase + Ly::OFF_RING;
+  RingPos rp;
+  uint32_t tile_ctr = 0, units = 0;
+  bool ok = true;
+#ifdef CPATTN_SERIALIZE_MMA
+  // Race-detection build: every MMA group completes before the MMA thread
+  // moves on (see prefill.cuh).
+  uint32_t ser_phase = 0;
+  auto serialize = [&]() {
+    mma2_commit_mc(bar(Ly::B_DRAIN), 0x1);
+    mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+    ser_phase ^= 1u;
+  };
+#else
+  auto serialize = []() {};
+  const uint32_t ser_phase = 0;
+#endif
+
+  // O (+)= P_w V_w over both CTAs' rows, P_w from the S buffer of tile t.
+  auto issue_pv = [&](int w, uint32_t t) {
+    const uint32_t sb = t & 1u;
+    if (!wait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
+    tc_fence_after();
+    const uint32_t p_tmem = tmem + HD + sb * kBKV;
+    for (int j = 0; j < Pl::VSLOTS; ++j) {
+      if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
+      tc_fence_after();
+      const uint32_t vb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
+#pragma unroll
+      for (int kk = 0; kk < Pl::VR / 16; ++kk) {
+        // V: VCH column chunks of VR rows x 128 B (chunk stride VR * 128),
+        // 16 key rows per step.
+        const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, Pl::VR * 128, 1024);
+        const int e0 = j * Pl::VR + kk * 16;
+        const uint32_t pa = p_tmem + 32 * (e0 >> 5) + ((e0 & 31) >> 1);
+        mma2_ts(tmem, pa, bd, Pl::IDESC_PV, (w | j | kk) != 0);
+        if (SPLIT) mma2_ts(tmem, pa + 16, bd, Pl::IDESC_PV, 1u);
+      }
+      serialize();
+      mma2_commit_mc(bar(Ly::B_SLOTEMPTY + rp.slot), 0x3);
+      rp.template advance<Ly::NSLOT>();
+    }
+    mma2_commit_mc(bar(Ly::B_ODONE + static_cast<int>(t & 1u)), 0x3);
+    return true;
+  };
+
+  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
+    const Unit U = decode_unit(p, u);
+    if (!wait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    for (int v = 0; v < U.n_tiles; ++v) {
+      const uint32_t sb = tile_ctr & 1u;
+      const uint32_t s_tmem = tmem + HD + sb * kBKV;
+      for (int j = 0; j < Pl::KSLOTS; ++j) {
+        if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c = 2 * j + c2;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = make_sdesc_sw128(q_base + c * (kBQ * 128) + kk * 32, 16, 1024);
+            const uint64_t bd = make_sdesc_sw128(kb + c2 * Pl::BOX + kk * 32, 16, 1024);
+            mma2_ss(s_tmem, ad, bd, Pl::IDESC_QK, (c | kk) != 0);
+          }
+        }
+        serialize();
+        mma2_commit_mc(bar(Ly::B_SLOTEMPTY + rp.slot), 0x3);
+        rp.template advance<Ly::NSLOT>();
+      }
+      if (!ok) break;
+      mma2_commit_mc(bar(Ly::B_SFULL + sb), 0x3);
+      if (v == U.n_tiles - 1) mma2_commit_mc(bar(Ly::B_QEMPTY), 0x3);
+      if (v >= 1 && !issue_pv(v - 1, tile_ctr - 1)) {
+        ok = false;
+        break;
+      }
+      ++tile_ctr;
+    }
+    if (ok) ok = issue_pv(U.n_tiles - 1, tile_ctr - 1);
+  }
+  // Every MMA issued must complete before either CTA releases its TMEM.
+  mma2_commit_mc(bar(Ly::B_DRAIN), 0x1);
+  mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+}
+
+// ------------------------------------------------------------------ kernel
+// Launched with clusters of two CTAs; CTA 2k + r runs units u = 2k + r +
+// m * gridDim.x, so the pair always holds q heads 2i and 2i + 1 of the same
+// row block (the host launches it only when the group size is even).
+template <int HD, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel_pair2(const __grid_constant__ PrefillParams p) {
+  using Ly = Layout<HD>;
+  using Pl = PairLayout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Ly::NBAR; ++i) {
+      uint32_t count = 1;
+      if (i == Ly::B_QFULL || (i >= Ly::B_SLOTFULL && i < Ly::B_SLOTEMPTY)) count = 2;
+      if (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) count = Pl::P_ARRIVALS;
+      mbar_init(bar(i), count);
+    }
+    *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) reinterpret_cast<volatile int*>(smem + Ly::OFF_PFAIL)[i] = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k_new_h);
+    prefetch_tmap(&p.tm_k_cache_h);
+    prefetch_tmap(&p.tm_v_new_h);
+    prefetch_tmap(&p.tm_v_cache_h);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Ly::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  // Both CTAs' barriers are initialised before any copy or arrival crosses.
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
+
+  if (warp < kProducerWarp) {
+    softmax_role<HD, SPLIT, true>(p, sbase, tmem, wait);
+  } else if (warp == kProducerWarp) {
+    if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
+  } else if (rank == 0) {
+    if (lane == 0) mma_role_pair2<HD, SPLIT>(p, sbase, tmem, wait);
+  }
+  __syncwarp();
+  tc_fence_before();
+  // The leader's MMAs (which write both CTAs' TMEM) have drained and both
+  // CTAs' softmax warps are done with TMEM before either CTA releases it.
+  cluster_sync();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, Ly::TMEM_COLS);
+  }
+  // Neither CTA leaves while the other may still arrive on its barriers.
+  cluster_sync();
+}
+
+}  // namespace cpattn

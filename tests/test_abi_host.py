@@ -65,6 +65,20 @@ def test_create_rejects(lib, cfg, status):
     assert e.value.status == status
 
 
+@pytest.mark.parametrize("value,ok", [("mma2", True), ("multicast", True), ("none", True),
+                                      ("both", False), ("", False)])
+def test_pairing_mode_from_environment(lib, monkeypatch, value, ok):
+    """CPATTN_PAIRING is read at create; an unknown value is rejected there
+    rather than silently running another kernel."""
+    monkeypatch.setenv("CPATTN_PAIRING", value)
+    if ok:
+        cp.Context(8, 2, 128, 2, 64, 32).close()
+    else:
+        with pytest.raises(cp.CpattnError) as e:
+            cp.Context(8, 2, 128, 2, 64, 32)
+        assert e.value.status == cp.E_INVALID
+
+
 def test_prefill_and_write_validation(lib):
     ctx = cp.Context(8, 2, 128, 2, 64, 32)
     A = 256  # a 16-byte-aligned stand-in pointer; nothing is launched

@@ -1,0 +1,69 @@
+"""The three CTA pairing modes of the fused prefill against the fp64 oracle.
+
+With an even group size the library pairs the CTAs of adjacent q heads of
+one kv head.  CPATTN_PAIRING (read when a context is created) picks how:
+'mma2' -- the leader CTA issues 2-SM MMAs (M = 256) and each CTA stages half
+of every K/V tile; 'multicast' -- each CTA issues its own MMAs and the pair
+shares K/V loads by multicast; 'none' -- one CTA per unit.  Every mode must
+meet the same bar on cases with several tiles, ragged chunks and an empty
+cache, in both P precisions."""
+import numpy as np
+import pytest
+
+import long_context_chunked_gb300 as cp
+from gpu_helpers import DeviceCase, compare, to_f64
+from helpers import make_case
+from workloads import small
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["mma2", "multicast", "none"]
+CASES = [
+    small("pairA", (0, 1000, 129), (300, 130, 256), 320, nq=8, nkv=2, hd=128, shards=4,
+          shard_capacity=300, seed=41),
+    small("pairB", (2500, 77), (384, 1), 384, nq=4, nkv=1, hd=256, shards=8, seed=42),
+    small("pairC", (5000,), (512,), 512, nq=8, nkv=2, hd=256, shards=8, seed=43,
+          peaky_frac=0.02),
+]
+
+
+@pytest.mark.parametrize("fast_p", [False, True], ids=["accurate", "fast_p"])
+@pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
+@pytest.mark.parametrize("mode", MODES)
+def test_pairing_mode_parity(mode, w, fast_p, monkeypatch):
+    monkeypatch.setenv("CPATTN_PAIRING", mode)
+    case = make_case(w)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w, fast_p=fast_p)
+    dc.prefill(ctx)
+    ref, ref_lse = case.oracle_full()
+    v = dc.valid_rows()
+    out = to_f64(dc.out.bits())
+    if fast_p:
+        # bf16 P (an option outside the parity bar): its rounding alone puts
+        # the relative RMS near 2.3e-3, so the check is looser.
+        compare(out[v], ref[v], f"{mode} {w.name} fast_p", max_abs_bar=2e-2, rel_bar=3.5e-3)
+    else:
+        compare(out[v], ref[v], f"{mode} {w.name}")
+    lse = dc.lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse[v] - ref_lse[v])) < 2e-3, "LSE"
+    pad = ~v
+    if pad.any():
+        assert np.all(dc.out.bits()[pad] == np.uint16(0x7F7F)), "pad rows written"
+    assert dc.guards_intact(), "write outside a buffer"
+
+
+def test_pairing_modes_repeatable(monkeypatch):
+    """Each mode gives identical bits on a second launch (a race in the
+    pair's cross-CTA barriers would show up as run-to-run differences)."""
+    w = CASES[2]
+    case = make_case(w)
+    dc = DeviceCase(case)
+    for mode in MODES:
+        monkeypatch.setenv("CPATTN_PAIRING", mode)
+        ctx = cp.Context.for_workload(w)
+        dc.prefill(ctx)
+        first = dc.out.bits().copy()
+        for _ in range(3):
+            dc.prefill(ctx)
+            assert np.array_equal(first, dc.out.bits()), mode
