@@ -44,25 +44,43 @@ def load_peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
-def csrc_hash() -> str:
+# Device sources each profiled kernel is built from (its launch code too).
+KERNEL_SOURCES = {
+    "prefill": ("cpattn.cu", "prefill.cuh", "prefill_pair.cuh", "walk.cuh", "ptx.cuh"),
+    "write_kv": ("cpattn.cu", "write_kv.cuh"),
+}
+
+
+def csrc_hash(kernel: str) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "long_context_chunked_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(d, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
+def prefill_kernel_name(w) -> str:
+    """The prefill kernel the library launches for this workload: paired CTAs
+    (CPATTN_PAIRING, default 2-SM MMA) when the group size is even."""
+    mode = os.environ.get("CPATTN_PAIRING", "mma2") if w.group % 2 == 0 else "none"
+    if mode == "mma2":
+        return "prefill_kernel_pair2<%d>" % w.head_dim
+    if mode == "multicast":
+        return "prefill_kernel<%d> (multicast pairs)" % w.head_dim
+    return "prefill_kernel<%d>" % w.head_dim
+
+
+def profiled_traffic(kernel: str, key: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(f"{kernel}:{workload}")
+            rec = json.load(f).get(key)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("csrc_hash") != csrc_hash():
+    if not rec or rec.get("csrc_hash") != csrc_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -293,14 +311,14 @@ def cpu_sample(w: Workload, budget_rows: int = 384, heads: int = 2):
     vc = oracle.build_striped_cache([oracle.bf16_bits(inp.v_cache[0][:, :1])], 1, w.shards,
                                     w.shard_capacity, hd, 0)
     kcf, vcf = oracle.bits_to_f64(kc), oracle.bits_to_f64(vc)
+    threads = min(heads, os.cpu_count() or 1)
     t0 = time.perf_counter()
-    oracle.attend_ref(q, kn, vn, kcf, vcf, [L], [rows], w.chunk, w.scale,
-                      threads=min(heads, os.cpu_count() or 1))
+    oracle.attend_ref(q, kn, vn, kcf, vcf, [L], [rows], w.chunk, w.scale, threads=threads)
     dt = time.perf_counter() - t0
     flops = 4 * hd * heads * (rows * L + rows * (rows + 1) // 2)
     desc = (f"{w.name}: sequence 0, {heads} q heads of kv head 0, chunk rows 0..{rows - 1}, "
-            f"full cache of {L} tokens ({flops / 1e9:.1f} GFLOP)")
-    return flops / dt / 1e12, dt, desc
+            f"full cache of {L} tokens ({flops / 1e9:.1f} GFLOP), {threads} worker threads")
+    return flops / dt / 1e12, dt, desc, threads
 
 
 # ------------------------------------------------------------------- main
@@ -331,11 +349,11 @@ def run_reference(args, world, rank):
     for _ in range(args.warmup):
         cpu_sample(w, budget_rows=args.ref_rows)
     for _ in range(args.steps):
-        tf, dt, desc = cpu_sample(w, budget_rows=args.ref_rows)
+        tf, dt, desc, threads = cpu_sample(w, budget_rows=args.ref_rows)
         vals.append((tf, dt))
     v = statistics.median(t for t, _ in vals)
     sec = statistics.median(d for _, d in vals)
-    cores = os.cpu_count() or 1
+    cores = threads
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -453,6 +471,7 @@ def main():
     e2e_ms, h2d, d2h = time_e2e(st, max(4, args.steps // 2), args.warmup)
 
     flops = w.attention_flops()
+    kname = prefill_kernel_name(w)
     ms_step = total_ms / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
@@ -476,8 +495,9 @@ def main():
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"bf16 dense burst, {peak_kind}",
                      "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
-                     "kernel": "prefill_kernel<%d>" % w.head_dim,
-                     "traffic": profiled_traffic("prefill", w.name)},
+                     "kernel": kname,
+                     "traffic": profiled_traffic(
+                         "prefill", f"{kname}:{w.name}:{'fast_p' if args.fast_p else 'accurate'}")},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
@@ -485,10 +505,12 @@ def main():
         "gpu_launches": (2 if args.variant == "fused" else 4) * args.steps,
         "clocks": clk.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        tf, dt, desc = cpu_sample(w)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # About 10 s of oracle work on a 16-core host: up to 16 q heads of kv
+        # head 0 (one worker thread each) and up to 2048 chunk rows.
+        tf, dt, desc, threads = cpu_sample(w, budget_rows=2048, heads=min(16, w.group))
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s",
-                                "cores": os.cpu_count() or 1, "kind": "oracle", "sample": desc,
+                                "cores": threads, "kind": "oracle", "sample": desc,
                                 "seconds": round(dt, 2)}
     if rank == 0:
         print(json.dumps(line), flush=True)
