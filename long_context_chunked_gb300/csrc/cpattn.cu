@@ -368,6 +368,10 @@ cpattn_status cpattn_sync_status(cpattn_ctx* ctx, void* stream) {
   if (e != cudaSuccess) return cuda_fail(ctx, e, "reading the status word");
   if (word != 0) {
     cudaMemset(ctx->d_status, 0, sizeof(int));
+    if ((word & 0xFF) == cpattn::kStatusLayout)
+      return fail(ctx, CPATTN_E_CUDA,
+                  "the kernel's dynamic shared memory base was not aligned as required; "
+                  "it returned without computing");
     return fail(ctx, CPATTN_E_TIMEOUT,
                 "a bounded device wait expired (site " + std::to_string(word >> 8) + ")");
   }

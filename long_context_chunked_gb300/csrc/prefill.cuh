@@ -68,11 +68,19 @@ struct PrefillParams {
 
 enum : int { kDebugDropArrive = 1 };
 
-// Warp roles: 0-7 softmax (two warpgroups), 8 TMA producer, 9 TMEM + MMA.
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
-constexpr uint32_t kSoftmaxThreads = 256;
+// Warp roles: 0 .. 4*kColGroups-1 softmax, then the TMA producer, then TMEM +
+// MMA.  Softmax warps w and w + 4k (k < kColGroups) hold the same 32 rows
+// (TMEM lane quarter w % 4) and split each row's 128 columns between them.
+// Two groups (8 softmax warps): four groups measured 3-8 % slower, since the
+// softmax is bound by instruction issue, not latency, and every extra warp
+// repeats the per-tile scalar work.
+constexpr int kColGroups = 2;
+constexpr int kSoftmaxWarps = 4 * kColGroups;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr uint32_t kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr uint32_t kRowGroupThreads = 32 * kColGroups;  // one named barrier per row group
 
 // Sites recorded in the status word when a bounded wait expires.
 enum : int {
@@ -97,9 +105,12 @@ struct Layout {
                        B_DRAIN = 8, B_SLOTFULL = 9, B_SLOTEMPTY = 9 + NSLOT;
   static constexpr int NBAR = 9 + 2 * NSLOT;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_XCH = OFF_MISC + 16;           // [2][128] fp32 row exchange
-  static constexpr int OFF_PFAIL = OFF_XCH + 1024;         // [4] int: a pair member gave up
-  static constexpr int SMEM_BYTES = OFF_PFAIL + 16 + 1024;  // + slack to align the base
+  static constexpr int OFF_XCH = OFF_MISC + 16;  // [kColGroups][128] fp32 row exchange
+  static constexpr int OFF_PFAIL = OFF_XCH + kColGroups * 128 * 4;  // [4] int: a row group gave up
+  // Slack for aligning the dynamic shared memory base to 1024 B; the kernel
+  // checks at entry that its base needs no more (it is 0 in practice).
+  static constexpr int ALIGN_SLACK = 512;
+  static constexpr int SMEM_BYTES = OFF_PFAIL + 16 + ALIGN_SLACK;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_QK = make_idesc_bf16(kBQ, kBKV, false);
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(kBQ, HD, true);
@@ -364,10 +375,11 @@ __device__ __forceinline__ uint32_t causal_word(int lim, int q) {
 }
 
 // ------------------------------------------------------- softmax + epilogue
-// Two warpgroups share the 128 rows: warp w (0..7) reads TMEM lanes
-// 32*(w%4).. (its rows) and owns half h = w/4 of every row's columns --
-// S columns [64h, 64h+64), O columns [h*HD/2, (h+1)*HD/2).  Warps w and w^4
-// hold the same rows; they agree on the row max through a paired barrier.
+// kColGroups warpgroups share the 128 rows: warp w reads TMEM lanes
+// 32*(w%4).. (its rows) and owns column group h = w/4 of every row -- S
+// columns [CW*h, CW*h + CW) with CW = 128 / kColGroups, O columns
+// [h*HD/kColGroups, (h+1)*HD/kColGroups).  The kColGroups warps holding the
+// same rows (a row group) agree on the row max through one named barrier.
 // PAIR2: the CTA is one of a pair whose leader issues 2-SM MMAs; S, P and O
 // of this CTA's 128 rows sit in its own TMEM exactly as in a single CTA, but
 // "P ready" goes to the leader's barrier, one arrival per warp.
@@ -376,29 +388,33 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
                                              const BoundedWait& wait) {
   using Ly = Layout<HD>;
   auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  constexpr int NG = kColGroups;
+  constexpr int CW = kBKV / NG;   // S columns per warp
+  constexpr int CH = CW / 32;     // 32-column TMEM loads per warp
   const int warp = threadIdx.x >> 5;
-  const int h = warp >> 2;                              // column half
+  const int h = warp >> 2;                              // column group
   const int r = ((warp & 3) << 5) | (threadIdx.x & 31);  // row == TMEM lane
-  const uint32_t pair_bar = 1u + static_cast<uint32_t>(warp & 3);  // named barrier of the pair
+  const uint32_t pair_bar = 1u + static_cast<uint32_t>(warp & 3);  // named barrier of the row group
   const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(r & ~31) << 16);
   float* xch = reinterpret_cast<float*>(
-      __cvta_shared_to_generic(sbase + Ly::OFF_XCH));   // [2][128] exchange slots
-  // A warp whose bounded wait expired must not leave while its partner may
-  // still reach a pair barrier: it raises the pair's flag and keeps going to
-  // the next pair barrier, after which both read the flag and leave together.
+      __cvta_shared_to_generic(sbase + Ly::OFF_XCH));   // [NG][128] exchange slots
+  // A warp whose bounded wait expired must not leave while the rest of its
+  // row group may still reach their barrier: it raises the group's flag and
+  // keeps going to the next group barrier, after which all read the flag and
+  // leave together.
   volatile int* pair_fail = reinterpret_cast<volatile int*>(
       __cvta_shared_to_generic(sbase + Ly::OFF_PFAIL)) + (warp & 3);
   const float sl2 = p.scale_log2;
   uint32_t tile_ctr = 0;
   bool drop_one = (p.debug_flags & kDebugDropArrive) && blockIdx.x == 0 && threadIdx.x == 0;
-  constexpr int OCOLS = HD / 2;                         // O columns of this half
+  constexpr int OCOLS = HD / NG;                        // O columns of this group
 
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     const Unit U = decode_unit(p, u);
     CacheWalk walk;
     walk.init(U.L, p.P, p.S);
     float m = -INFINITY;  // running reference max of the scaled logits (log2 units), per row
-    float l = 0.f;        // this half's running sum of 2^(x - m)
+    float l = 0.f;        // this group's running sum of 2^(x - m)
     bool ok = true;
     bool left_at_vote = false;  // the only way out of the tile loop before its end
 
@@ -406,9 +422,9 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       const uint32_t sb = tile_ctr & 1u;
       ok = wait(bar(Ly::B_SFULL + sb), (tile_ctr >> 1) & 1u, kSiteSFull);
       ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) *pair_fail = 1;  // decided at the vote below, together with the partner
+      if (!ok) *pair_fail = 1;  // decided at the vote below, together with the group
       tc_fence_after();
-      const uint32_t s_tmem = lane_tmem + HD + sb * kBKV + 64 * h;
+      const uint32_t s_tmem = lane_tmem + HD + sb * kBKV + CW * h;
 
       // Region by value: one scalar picks the validity words of the tile.
       const bool in_cache = v < U.n_cache;
@@ -425,49 +441,63 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 #pragma unroll
         for (int q = 0; q < 4; ++q) mw[q] = causal_word(lim, q);
       }
-      const uint32_t w0 = h ? mw[2] : mw[0], w1 = h ? mw[3] : mw[1];
-      const bool need_mask = __any_sync(0xFFFFFFFFu, (w0 & w1) != 0xFFFFFFFFu);
+      uint32_t wq[CH];
+      uint32_t all_valid = 0xFFFFFFFFu;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int idx = h * CH + c;  // selected by value: no local-memory array
+        uint32_t wv = mw[0];
+#pragma unroll
+        for (int k = 1; k < 4; ++k) wv = (idx == k) ? mw[k] : wv;
+        wq[c] = wv;
+        all_valid &= wv;
+      }
+      const bool need_mask = __any_sync(0xFFFFFFFFu, all_valid != 0xFFFFFFFFu);
 
-      // Pass 1: load this half's 64 logits (two 32-column TMEM loads in
-      // flight together), mask by value, and take their max.  The registers
-      // stay live for pass 2.
-      uint32_t ra[32], rb[32];
-      tmem_ld32_async(s_tmem, ra);
-      tmem_ld32_async(s_tmem + 32, rb);
-      tmem_ld32_fence(ra);
-      tmem_ld32_fence(rb);
+      // Pass 1: load this group's CW logits (all TMEM loads in flight
+      // together), mask by value, and take their max.  The registers stay
+      // live for pass 2.
+      uint32_t rr[CH][32];
+#pragma unroll
+      for (int c = 0; c < CH; ++c) tmem_ld32_async(s_tmem + 32 * c, rr[c]);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) tmem_ld32_fence(rr[c]);
       if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          ra[i] = ((w0 >> i) & 1u) ? ra[i] : 0xFF800000u;  // -inf
-          rb[i] = ((w1 >> i) & 1u) ? rb[i] : 0xFF800000u;
-        }
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            rr[c][i] = ((wq[c] >> i) & 1u) ? rr[c][i] : 0xFF800000u;  // -inf
       }
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        mx0 = fmaxf(mx0, __uint_as_float(ra[i]));
-        mx1 = fmaxf(mx1, __uint_as_float(ra[i + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(rb[i]));
-        mx3 = fmaxf(mx3, __uint_as_float(rb[i + 1]));
-      }
+      for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(rr[c][i]));
+          mx1 = fmaxf(mx1, __uint_as_float(rr[c][i + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(rr[c][i + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(rr[c][i + 3]));
+        }
       const float m_half = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
 
       // Lazy rescale: the reference max moves only when a row's new logits
       // exceed it by more than 2^8 (the final O / l is the same either way).
-      // The pair votes; only then do the halves exchange their maxima.
+      // The row group votes; only then do the groups exchange their maxima.
       float alpha = 1.f;
       bool warp_rescale = false;
-      const bool any_need =
-          bar_red_or(pair_bar, 64, !ok || *pair_fail != 0 || v == 0 || m_half > m + 8.f);
+      const bool any_need = bar_red_or(pair_bar, kRowGroupThreads,
+                                       !ok || *pair_fail != 0 || v == 0 || m_half > m + 8.f);
       if (any_need) {
-        if (*pair_fail) {  // read by both warps after the same barrier
+        if (*pair_fail) {  // read by every warp of the group after the same barrier
           left_at_vote = true;
           break;
         }
         xch[h * 128 + r] = m_half;
-        bar_sync(pair_bar, 64);
-        const float m_tile = fmaxf(m_half, xch[(h ^ 1) * 128 + r]);
+        bar_sync(pair_bar, kRowGroupThreads);
+        float m_tile = xch[r];
+#pragma unroll
+        for (int g = 1; g < NG; ++g) m_tile = fmaxf(m_tile, xch[g * 128 + r]);
         const float m_new = fmaxf(m, m_tile);
         const bool need = (v > 0) && (m_new > m + 8.f);
         alpha = need ? ex2_approx(m - m_new) : 1.f;
@@ -475,7 +505,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
         if (v == 0 || need) m = m_new;
       }
 
-      // Pass 2: p = 2^(x - m) and this half's row sum.  Chunk q (32 keys)
+      // Pass 2: p = 2^(x - m) and this group's row sum.  Chunk q (32 keys)
       // holds, over its own 32 columns of the S buffer, P_hi = bf16(p) in the
       // first 16 and -- accurate mode -- P_lo = bf16(p - P_hi) in the next 16.
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
@@ -504,8 +534,8 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
           tmem_st16(s_tmem + 32 * q, hi);
           if (SPLIT) tmem_st16(s_tmem + 32 * q + 16, lo);
         };
-        chunk_exp(ra, 0);
-        chunk_exp(rb, 1);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) chunk_exp(rr[c], c);
       }
       l = l * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
@@ -554,17 +584,19 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       }
       ++tile_ctr;
     }
-    if (left_at_vote) break;  // both warps of the pair left together
+    if (left_at_vote) break;  // every warp of the row group left together
 
-    // Epilogue: the pair adds its half sums (the first barrier keeps the
-    // partner's last read of the exchange slot ahead of this write, and
-    // settles a failure raised after the last vote); each half stores its O
-    // columns as bf16 (valid rows only).
-    bar_sync(pair_bar, 64);
+    // Epilogue: the row group adds its partial sums (the first barrier keeps
+    // the other warps' last reads of the exchange slots ahead of this write,
+    // and settles a failure raised after the last vote); each group stores
+    // its O columns as bf16 (valid rows only).
+    bar_sync(pair_bar, kRowGroupThreads);
     if (*pair_fail) break;
     xch[h * 128 + r] = l;
-    bar_sync(pair_bar, 64);
-    const float l_row = l + xch[(h ^ 1) * 128 + r];
+    bar_sync(pair_bar, kRowGroupThreads);
+    float l_row = xch[r];
+#pragma unroll
+    for (int g = 1; g < NG; ++g) l_row += xch[g * 128 + r];
     const uint32_t t_last = tile_ctr - 1;  // its commit covers every earlier MMA too
     ok = wait(bar(Ly::B_ODONE + static_cast<int>(t_last & 1u)), (t_last >> 1) & 1u, kSiteODone);
     ok = __all_sync(0xFFFFFFFFu, ok);
@@ -616,6 +648,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
+  if (sbase - raw > static_cast<uint32_t>(Ly::ALIGN_SLACK)) {  // never seen; refuse, do not overrun
+    if (threadIdx.x == 0 && p.status != nullptr) atomicCAS(p.status, kStatusOk, kStatusLayout);
+    return;
+  }
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::OFF_MISC + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

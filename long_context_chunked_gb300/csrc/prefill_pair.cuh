@@ -265,6 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
+  // Same base offset in both CTAs (same kernel), so both leave here together.
+  if (sbase - raw > static_cast<uint32_t>(Ly::ALIGN_SLACK)) {
+    if (threadIdx.x == 0 && p.status != nullptr) atomicCAS(p.status, kStatusOk, kStatusLayout);
+    return;
+  }
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Ly::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::OFF_MISC + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -79,7 +79,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluste
 }
 
 // Device status word codes (written by the first role that gives up).
-enum : int { kStatusOk = 0, kStatusTimeout = 1 };
+enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusLayout = 2 };
 
 // A wait with a wall-clock limit.  On expiry it records the site in the
 // device status word, raises the CTA-wide abort flag and returns false; a
