@@ -119,8 +119,13 @@ cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* 
  *   out                 device bf16 [B*C, NQ, HD]; pad rows are not written
  *   lse                 device fp32 [B*C, NQ] natural-log sum-exp of the
  *                       scaled logits, or NULL; pad rows not written
- * Errors: E_INVALID, E_UNSUPPORTED (more than CPATTN_MAX_ROW_BLOCKS row
- * blocks), E_CUDA.  A device-side timeout is reported by cpattn_sync_status.
+ * One kernel launch -- unless a split-KV workspace is registered
+ * (cpattn_set_splitkv) and the batch's plan cuts some walks, in which case a
+ * second, merge kernel follows on the same stream.
+ * Errors: E_INVALID (also: the registered split-KV workspace is smaller than
+ * the plan needs), E_UNSUPPORTED (more than CPATTN_MAX_ROW_BLOCKS row blocks,
+ * a walk of more than 65535 tiles), E_CUDA.  A device-side timeout is
+ * reported by cpattn_sync_status.
  */
 cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
                              const int32_t* chunk_lens, const void* q, const void* k_new,
@@ -147,6 +152,51 @@ cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
                                         const void* k_cache, const void* v_cache, void* out,
                                         float* lse, void* workspace, uint64_t workspace_bytes,
                                         void* stream);
+
+/*
+ * Split-KV for small chunks and decode.  With few row blocks (a short chunk,
+ * or a decode step of one token) most SMs would idle while a few units walk
+ * a long cache.  Once a workspace is registered here, cpattn_prefill may cut
+ * a row block's tile walk (its cache tiles, then its causal current tiles)
+ * into pieces run on different SMs.  Each piece writes fp32 O / l and its LSE
+ * for the block's valid rows into the workspace.  A second kernel on the same
+ * stream combines the pieces of each row by their LSE (the merge of the
+ * two-launch variant above, generalised to n pieces) into bf16 `out` and `lse`.
+ * The result is the same softmax over the same keys.  This is the single-GPU
+ * counterpart of the pages' spilled running (m, l, acc) for very long
+ * contexts (PCP ring-cache PR, Design section).
+ *   workspace        device memory owned by the caller, 256-byte aligned,
+ *                    used by every later cpattn_prefill of this context on
+ *                    its stream until replaced; NULL turns split-KV off
+ *                    (the default).  Calls that overlap on the GPU must not
+ *                    share one workspace.
+ *   workspace_bytes  its size; a prefill whose plan needs more fails with
+ *                    E_INVALID (query the need with cpattn_splitkv_workspace)
+ *   max_split_tiles  0: automatic -- walks are cut only when the longest one
+ *                    exceeds 1.25x the average work per SM, into pieces of
+ *                    about that average (at least 16 tiles); > 0: every walk
+ *                    longer than this many tiles is cut into pieces of at
+ *                    most this many (for tests and tuning)
+ * Limits: at most 256 row blocks are cut per call (the longest ones), and
+ * the pieces count against CPATTN_MAX_ROW_BLOCKS.
+ * Errors: E_INVALID (NULL ctx, max_split_tiles < 0, misaligned workspace).
+ */
+cpattn_status cpattn_set_splitkv(cpattn_ctx* ctx, void* workspace, uint64_t workspace_bytes,
+                                 int32_t max_split_tiles);
+
+/*
+ * Workspace bytes the split-KV plan of this batch needs under the policy
+ * `max_split_tiles` (as in cpattn_set_splitkv), written to *bytes (0 when
+ * nothing would be split).  *work_blocks (if not NULL) receives the number of
+ * work blocks the kernel would run: the row blocks, plus one for every extra
+ * piece.  Host only; reads the sequence arrays during the call.
+ * Errors: E_INVALID (as cpattn_prefill's sequence checks, NULL bytes),
+ * E_UNSUPPORTED (the plan exceeds the kernel's tables).
+ */
+cpattn_status cpattn_splitkv_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
+                                       const int32_t* cache_lens, const int32_t* chunk_lens,
+                                       int32_t max_split_tiles, uint64_t* bytes,
+                                       int32_t* work_blocks);
 
 /*
  * Synchronise `stream`, then read and clear the context's device status word.
@@ -176,6 +226,16 @@ cpattn_status cpattn_set_fault_injection(cpattn_ctx* ctx, int32_t flags, int32_t
  */
 cpattn_status cpattn_cache_walk(const cpattn_ctx* ctx, int32_t cache_len, int32_t* tiles,
                                 uint32_t* masks, int32_t max_tiles, int32_t* count);
+
+/*
+ * The same view of the walk from its tile `first` on (first >= 0): the tiles
+ * a split-KV piece that starts at virtual tile `first` visits, found by
+ * skipping whole shard ranges as the kernel does.  Errors as above, and
+ * E_INVALID for first < 0.
+ */
+cpattn_status cpattn_cache_walk_from(const cpattn_ctx* ctx, int32_t cache_len, int32_t first,
+                                     int32_t* tiles, uint32_t* masks, int32_t max_tiles,
+                                     int32_t* count);
 
 /*
  * Allocation-free fused prefill.  The pages have no counterpart for this

@@ -24,7 +24,8 @@ MAX_ROW_BLOCKS = 2048
 EXPORTS = ("cpattn_create", "cpattn_write_kv", "cpattn_prefill", "cpattn_sync_status",
            "cpattn_set_fault_injection", "cpattn_cache_walk", "cpattn_destroy",
            "cpattn_status_string", "cpattn_last_error", "cpattn_prefill_noalloc",
-           "cpattn_two_launch_workspace", "cpattn_prefill_two_launch")
+           "cpattn_two_launch_workspace", "cpattn_prefill_two_launch", "cpattn_set_splitkv",
+           "cpattn_splitkv_workspace", "cpattn_cache_walk_from")
 
 
 class CpattnError(RuntimeError):
@@ -78,6 +79,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cpattn_two_launch_workspace.restype = I32
     lib.cpattn_prefill_two_launch.argtypes = [P, I32, I32P, I32P] + [P] * 8 + [ctypes.c_uint64, P]
     lib.cpattn_prefill_two_launch.restype = I32
+    lib.cpattn_set_splitkv.argtypes = [P, P, ctypes.c_uint64, I32]
+    lib.cpattn_set_splitkv.restype = I32
+    lib.cpattn_splitkv_workspace.argtypes = [P, I32, I32P, I32P, I32,
+                                             ctypes.POINTER(ctypes.c_uint64), I32P]
+    lib.cpattn_splitkv_workspace.restype = I32
+    lib.cpattn_cache_walk_from.argtypes = [P, I32, I32, I32P, ctypes.POINTER(U32), I32, I32P]
+    lib.cpattn_cache_walk_from.restype = I32
     _lib = lib
     return lib
 
@@ -177,6 +185,23 @@ class Context:
             self._h, len(cl), clp, chp, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
             _ptr(v_cache), _ptr(out), _ptr(lse), _ptr(workspace), nbytes, _stream(stream)))
 
+    def set_splitkv(self, workspace=None, max_split_tiles: int = 0):
+        """Register a device workspace (a CUDA tensor, 256-byte aligned) for
+        split-KV, or None to turn it off; max_split_tiles 0 = automatic."""
+        nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self._check(self.lib.cpattn_set_splitkv(self._h, _ptr(workspace), nbytes,
+                                                max_split_tiles))
+
+    def splitkv_workspace(self, cache_lens, chunk_lens, max_split_tiles: int = 0):
+        """(workspace bytes, work blocks) of this batch's split-KV plan."""
+        cl, clp = _i32(cache_lens)
+        ch, chp = _i32(chunk_lens)
+        n = ctypes.c_uint64()
+        blocks = ctypes.c_int32()
+        self._check(self.lib.cpattn_splitkv_workspace(self._h, len(cl), clp, chp, max_split_tiles,
+                                                      ctypes.byref(n), ctypes.byref(blocks)))
+        return n.value, blocks.value
+
     def sync_status(self, stream=None) -> int:
         """Synchronise and return the status code (E_TIMEOUT if a device wait expired)."""
         return self.lib.cpattn_sync_status(self._h, _stream(stream))
@@ -184,15 +209,18 @@ class Context:
     def set_fault_injection(self, flags: int, timeout_ms: int = 0):
         self._check(self.lib.cpattn_set_fault_injection(self._h, flags, timeout_ms))
 
-    def cache_walk(self, cache_len: int):
-        """(tiles int32 [n], masks uint32 [n, 4]) of the kernel's cache walk."""
+    def cache_walk(self, cache_len: int, first: int = 0):
+        """(tiles int32 [n], masks uint32 [n, 4]) of the kernel's cache walk,
+        from its tile `first` on (the start of a split-KV piece)."""
         n = ctypes.c_int32()
-        self._check(self.lib.cpattn_cache_walk(self._h, cache_len, None, None, 0, ctypes.byref(n)))
+        fn = self.lib.cpattn_cache_walk_from
+        self._check(fn(self._h, cache_len, first, None, None, 0, ctypes.byref(n)))
         tiles = np.zeros(max(n.value, 1), dtype=np.int32)
         masks = np.zeros((max(n.value, 1), 4), dtype=np.uint32)
-        self._check(self.lib.cpattn_cache_walk(
-            self._h, cache_len, tiles.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-            masks.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), n.value, ctypes.byref(n)))
+        self._check(fn(self._h, cache_len, first,
+                       tiles.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                       masks.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), n.value,
+                       ctypes.byref(n)))
         return tiles[:n.value], masks[:n.value]
 
     def last_error(self) -> str:

@@ -20,6 +20,7 @@
 #include "walk.cuh"
 #include "write_kv.cuh"
 #include "merge.cuh"
+#include "plan.h"
 
 struct cpattn_ctx {
   cpattn_config cfg;
@@ -30,6 +31,11 @@ struct cpattn_ctx {
   // CTA pairing for even group sizes (CPATTN_PAIRING = mma2 | multicast | none):
   // 2 = 2-SM MMA pairs, 1 = pairs sharing K/V loads by multicast, 0 = off.
   int pair_mode = 2;
+  // Split-KV: a caller-owned device workspace and the policy (kSplitOff,
+  // kSplitAuto, or a forced piece length in tiles); off until registered.
+  void* split_ws = nullptr;
+  size_t split_ws_bytes = 0;
+  int split_policy = cpattn::kSplitOff;
   int debug_flags = 0;
   unsigned long long timeout_ns = 1000ull * 1000 * 1000;
   bool debug_sync = false;
@@ -172,37 +178,93 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
   return after_launch(ctx, stream, "prefill launch");
 }
 
-// Build the launch description of one prefill (all regions, or one region
-// for the two-launch variant) and launch it.  Arguments already validated.
+// SMs the persistent grid spans (the plan's notion of parallel slots; with
+// CTA pairs both the units and the slots halve, so the ratio is the same).
+int plan_slots(const cpattn_ctx* ctx) { return ctx->num_sms > 0 ? ctx->num_sms : 148; }
+
+cpattn_status dispatch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st) {
+  const int HD = ctx->cfg.head_dim;
+  const bool split = ctx->cfg.fast_p == 0;
+  // Pair CTAs on adjacent q heads of one kv head when the group size allows.
+  const int mode = (prm->group % 2 == 0) ? ctx->pair_mode : 0;
+  if (HD == 256) {
+    if (mode == 2) return split ? launch_prefill<256, true, 2>(ctx, prm, st)
+                                : launch_prefill<256, false, 2>(ctx, prm, st);
+    if (mode == 1) return split ? launch_prefill<256, true, 1>(ctx, prm, st)
+                                : launch_prefill<256, false, 1>(ctx, prm, st);
+    return split ? launch_prefill<256, true, 0>(ctx, prm, st)
+                 : launch_prefill<256, false, 0>(ctx, prm, st);
+  }
+  if (mode == 2) return split ? launch_prefill<128, true, 2>(ctx, prm, st)
+                              : launch_prefill<128, false, 2>(ctx, prm, st);
+  if (mode == 1) return split ? launch_prefill<128, true, 1>(ctx, prm, st)
+                              : launch_prefill<128, false, 1>(ctx, prm, st);
+  return split ? launch_prefill<128, true, 0>(ctx, prm, st)
+               : launch_prefill<128, false, 0>(ctx, prm, st);
+}
+
+// Combine the split-KV pieces of every split row block into the output.
+cpattn_status launch_splitkv_merge(cpattn_ctx* ctx, const cpattn::WorkPlan& plan,
+                                   const float* ws_o, const float* ws_lse, void* out, float* lse,
+                                   int32_t num_seqs, cudaStream_t st) {
+  static thread_local cpattn::SplitMergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  const cpattn_config& c = ctx->cfg;
+  mp.ws_o = ws_o;
+  mp.ws_lse = ws_lse;
+  mp.out = static_cast<__nv_bfloat16*>(out);
+  mp.lse = lse;
+  mp.C = c.chunk_size;
+  mp.nq = c.num_q_heads;
+  mp.hd = c.head_dim;
+  mp.num_groups = static_cast<int>(plan.groups.size());
+  long long total = 0;
+  for (int g = 0; g < mp.num_groups; ++g) {
+    const cpattn::SplitGroup& G = plan.groups[g];
+    mp.g_b[g] = G.b;
+    mp.g_q0[g] = G.q0;
+    mp.g_rows[g] = G.rows;
+    mp.g_n[g] = G.n;
+    mp.g_part0[g] = G.part0;
+    mp.g_prefix[g] = total;
+    total += static_cast<long long>(G.rows) * c.num_q_heads * (c.head_dim / 8);
+  }
+  mp.g_prefix[mp.num_groups] = total;
+  mp.total = total;
+  (void)num_seqs;
+  const long long want = (total + 255) / 256;
+  const int grid = static_cast<int>(std::max<long long>(
+      1, std::min<long long>(want, static_cast<long long>(std::max(ctx->num_sms, 1)) * 8)));
+  cpattn::splitkv_merge_kernel<<<grid, 256, 0, st>>>(mp);
+  return after_launch(ctx, st, "split-KV merge launch");
+}
+
+// Plan and launch one prefill: all regions (optionally split-KV, then the
+// merge), or one region of the two-launch variant.  Arguments already
+// validated.
 cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,
                              const int32_t* chunk_lens, const void* q, const void* k_new,
                              const void* v_new, const void* k_cache, const void* v_cache,
-                             void* out, float* lse, void* stream, int region, int out_f32) {
+                             void* out, float* lse, void* stream, int region, int out_f32,
+                             int split) {
   const cpattn_config& c = ctx->cfg;
-
-  // Row blocks (b, q block), longest first: a unit's cost is its tile count.
-  // region 1 (cache only) has no work for a sequence with an empty cache.
-  struct Blk { int work, b, qb; };
-  std::vector<Blk> blks;
-  std::vector<int> ncache(num_seqs);
-  for (int b = 0; b < num_seqs; ++b) {
-    ncache[b] = cpattn::cache_tile_count(cache_lens[b], c.num_shards, c.shard_capacity);
-    if (region == 1 && ncache[b] == 0) continue;
-    const int nqb = (chunk_lens[b] + kBQ - 1) / kBQ;
-    for (int qb = 0; qb < nqb; ++qb) {
-      const int work = (region == 2 ? 0 : ncache[b]) + (region == 1 ? 0 : qb + 1);
-      blks.push_back({work, b, qb});
-    }
-  }
-  if (blks.size() > CPATTN_MAX_ROW_BLOCKS)
-    return fail(ctx, CPATTN_E_UNSUPPORTED, "more than CPATTN_MAX_ROW_BLOCKS row blocks");
-  if (blks.empty()) return CPATTN_OK;
+  const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
+  static thread_local cpattn::WorkPlan plan;
+  std::string why;
+  if (!cpattn::make_plan(c, num_seqs, cache_lens, chunk_lens, region, split, plan_slots(ctx),
+                         &plan, &why))
+    return fail(ctx, CPATTN_E_UNSUPPORTED, why);
+  if (plan.blocks.empty()) return CPATTN_OK;
+  const size_t ws_need = cpattn::plan_workspace_bytes(plan, NQ, HD);
+  if (ws_need > ctx->split_ws_bytes)
+    return fail(ctx, CPATTN_E_INVALID,
+                "the registered split-KV workspace holds " + std::to_string(ctx->split_ws_bytes) +
+                    " bytes; this batch's plan needs " + std::to_string(ws_need) +
+                    " (cpattn_splitkv_workspace)");
   if (ctx->d_status == nullptr) return fail(ctx, CPATTN_E_CUDA, "no CUDA device");
-  std::stable_sort(blks.begin(), blks.end(), [](const Blk& a, const Blk& b) { return a.work > b.work; });
 
   static thread_local cpattn::PrefillParams prm;
   std::memset(&prm, 0, sizeof(prm));
-  const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
   const uint64_t T = static_cast<uint64_t>(num_seqs) * c.chunk_size;
   const uint64_t rows = static_cast<uint64_t>(num_seqs) * NKV * c.num_shards * c.shard_capacity;
   const uint32_t vrows = 8192u / static_cast<uint32_t>(HD);
@@ -219,8 +281,13 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   if (!ok) return fail(ctx, CPATTN_E_CUDA, "cuTensorMapEncodeTiled failed");
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
-  prm.region = region;
   prm.out_f32 = out_f32;
+  if (ws_need > 0) {
+    const size_t o_bytes =
+        cpattn::align256(static_cast<size_t>(plan.partial_rows) * NQ * static_cast<size_t>(HD) * 4);
+    prm.ws_o = static_cast<float*>(ctx->split_ws);
+    prm.ws_lse = reinterpret_cast<float*>(static_cast<char*>(ctx->split_ws) + o_bytes);
+  }
   prm.status = ctx->d_status;
   prm.timeout_ns = ctx->timeout_ns;
   prm.nq = NQ;
@@ -232,29 +299,19 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   prm.debug_flags = ctx->debug_flags;
   prm.scale_log2 = c.softmax_scale * 1.4426950408889634f;
   for (int b = 0; b < num_seqs; ++b)
-    prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], ncache[b], 0};
-  for (size_t i = 0; i < blks.size(); ++i)
-    prm.blocks[i] = (static_cast<uint32_t>(blks[i].b) << 16) | static_cast<uint32_t>(blks[i].qb);
-  prm.num_units = static_cast<int>(blks.size()) * NQ;
+    prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], plan.ncache[b], 0};
+  for (size_t i = 0; i < plan.blocks.size(); ++i) {
+    const cpattn::WorkBlock& w = plan.blocks[i];
+    prm.blocks[i] = (static_cast<uint32_t>(w.b) << 16) | static_cast<uint32_t>(w.qb);
+    prm.range[i] = (static_cast<uint32_t>(w.v0) << 16) | static_cast<uint32_t>(w.v1);
+    prm.part[i] = w.part;
+  }
+  prm.num_units = static_cast<int>(plan.blocks.size()) * NQ;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool split = c.fast_p == 0;
-  // Pair CTAs on adjacent q heads of one kv head when the group size allows.
-  const int mode = (prm.group % 2 == 0) ? ctx->pair_mode : 0;
-  if (HD == 256) {
-    if (mode == 2) return split ? launch_prefill<256, true, 2>(ctx, &prm, st)
-                                : launch_prefill<256, false, 2>(ctx, &prm, st);
-    if (mode == 1) return split ? launch_prefill<256, true, 1>(ctx, &prm, st)
-                                : launch_prefill<256, false, 1>(ctx, &prm, st);
-    return split ? launch_prefill<256, true, 0>(ctx, &prm, st)
-                 : launch_prefill<256, false, 0>(ctx, &prm, st);
-  }
-  if (mode == 2) return split ? launch_prefill<128, true, 2>(ctx, &prm, st)
-                              : launch_prefill<128, false, 2>(ctx, &prm, st);
-  if (mode == 1) return split ? launch_prefill<128, true, 1>(ctx, &prm, st)
-                              : launch_prefill<128, false, 1>(ctx, &prm, st);
-  return split ? launch_prefill<128, true, 0>(ctx, &prm, st)
-               : launch_prefill<128, false, 0>(ctx, &prm, st);
+  cpattn_status s = dispatch_prefill(ctx, &prm, st);
+  if (s != CPATTN_OK || plan.groups.empty()) return s;
+  return launch_splitkv_merge(ctx, plan, prm.ws_o, prm.ws_lse, out, lse, num_seqs, st);
 }
 
 }  // namespace
@@ -335,11 +392,19 @@ cpattn_status cpattn_set_fault_injection(cpattn_ctx* ctx, int32_t flags, int32_t
 
 cpattn_status cpattn_cache_walk(const cpattn_ctx* ctx, int32_t cache_len, int32_t* tiles,
                                 uint32_t* masks, int32_t max_tiles, int32_t* count) {
-  if (ctx == nullptr || count == nullptr || cache_len < 0 || max_tiles < 0) return CPATTN_E_INVALID;
+  return cpattn_cache_walk_from(ctx, cache_len, 0, tiles, masks, max_tiles, count);
+}
+
+cpattn_status cpattn_cache_walk_from(const cpattn_ctx* ctx, int32_t cache_len, int32_t first,
+                                     int32_t* tiles, uint32_t* masks, int32_t max_tiles,
+                                     int32_t* count) {
+  if (ctx == nullptr || count == nullptr || cache_len < 0 || max_tiles < 0 || first < 0)
+    return CPATTN_E_INVALID;
   const int P = ctx->cfg.num_shards, S = ctx->cfg.shard_capacity;
   if (static_cast<long long>(cache_len) > static_cast<long long>(P) * S) return CPATTN_E_INVALID;
   cpattn::CacheWalk w;
   w.init(cache_len, P, S);
+  w.skip(first);  // as a split-KV piece starting at virtual tile `first` does
   int n = 0;
   while (!w.done()) {
     const int t = w.next();
@@ -430,7 +495,36 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
       !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)))
     return fail(ctx, CPATTN_E_INVALID, "device pointers must be 16-byte aligned");
   return prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
-                        out, lse, stream, 0, 0);
+                        out, lse, stream, cpattn::kRegionAll, 0,
+                        ctx->split_ws != nullptr ? ctx->split_policy : cpattn::kSplitOff);
+}
+
+cpattn_status cpattn_set_splitkv(cpattn_ctx* ctx, void* workspace, uint64_t workspace_bytes,
+                                 int32_t max_split_tiles) {
+  if (ctx == nullptr || max_split_tiles < 0) return CPATTN_E_INVALID;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(ctx, CPATTN_E_INVALID, "split-KV workspace must be 256-byte aligned");
+  ctx->split_ws = workspace;
+  ctx->split_ws_bytes = workspace != nullptr ? static_cast<size_t>(workspace_bytes) : 0;
+  ctx->split_policy = workspace != nullptr ? max_split_tiles : cpattn::kSplitOff;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_splitkv_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
+                                       const int32_t* cache_lens, const int32_t* chunk_lens,
+                                       int32_t max_split_tiles, uint64_t* bytes,
+                                       int32_t* work_blocks) {
+  if (ctx == nullptr || bytes == nullptr || max_split_tiles < 0) return CPATTN_E_INVALID;
+  cpattn_status s = check_seqs(const_cast<cpattn_ctx*>(ctx), num_seqs, cache_lens, chunk_lens);
+  if (s != CPATTN_OK) return s;
+  cpattn::WorkPlan plan;
+  std::string why;
+  if (!cpattn::make_plan(ctx->cfg, num_seqs, cache_lens, chunk_lens, cpattn::kRegionAll,
+                         max_split_tiles, plan_slots(ctx), &plan, &why))
+    return CPATTN_E_UNSUPPORTED;
+  *bytes = cpattn::plan_workspace_bytes(plan, ctx->cfg.num_q_heads, ctx->cfg.head_dim);
+  if (work_blocks != nullptr) *work_blocks = static_cast<int32_t>(plan.blocks.size());
+  return CPATTN_OK;
 }
 
 // Two-launch variant: workspace = two fp32 partial outputs and two LSE rows.
@@ -485,10 +579,10 @@ cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
   float* l2 = reinterpret_cast<float*>(ws + off[3]);
   // Launch 1: cache tiles only; launch 2: current tiles only (causal).
   s = prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
-                     o1, l1, stream, 1, 1);
+                     o1, l1, stream, cpattn::kRegionCache, 1, cpattn::kSplitOff);
   if (s != CPATTN_OK) return s;
   s = prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
-                     o2, l2, stream, 2, 1);
+                     o2, l2, stream, cpattn::kRegionCurrent, 1, cpattn::kSplitOff);
   if (s != CPATTN_OK) return s;
   // Launch 3: LSE merge into bf16 O.
   cpattn::MergeParams m;
@@ -656,7 +750,13 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
     }
   }
   std::sort(keys, keys + n);
-  for (int i = 0; i < n; ++i) prm.blocks[i] = static_cast<uint32_t>(keys[i] & 0xFFFFFFFFull);
+  for (int i = 0; i < n; ++i) {
+    const uint64_t work = 0xFFFFFFFFull - (keys[i] >> 32);  // whole walk: [0, n_cache + qb + 1)
+    if (work > static_cast<uint64_t>(cpattn::kMaxVirtualTiles)) return CPATTN_E_UNSUPPORTED;
+    prm.blocks[i] = static_cast<uint32_t>(keys[i] & 0xFFFFFFFFull);
+    prm.range[i] = static_cast<uint32_t>(work);
+    prm.part[i] = -1;
+  }
 
   const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
   const uint64_t T = static_cast<uint64_t>(num_seqs) * c.chunk_size;

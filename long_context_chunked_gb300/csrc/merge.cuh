@@ -72,4 +72,72 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const __grid_constant__ 
   }
 }
 
+// Split-KV merge: a row block whose tile walk was cut into n pieces (a
+// "group") has, per valid row and q head, n partial results (O_s / l_s in
+// fp32 and LSE_s) over disjoint key sets; the softmax over their union is
+//   m = max_s LSE_s,  w_s = exp(LSE_s - m),
+//   O = sum_s w_s O_s / sum_s w_s,  LSE = m + log(sum_s w_s).
+// Piece s of a group has its partial rows at part0 + s * rows.  HBM-bound:
+// one thread per 8 consecutive output elements of one (row, head).
+constexpr int kMaxSplitGroups = 256;
+
+struct SplitMergeParams {
+  const float* ws_o;    // [partial rows][NQ][HD]
+  const float* ws_lse;  // [partial rows][NQ]
+  __nv_bfloat16* out;   // [T, NQ, HD]
+  float* lse;           // [T, NQ] or null
+  int num_groups, C, nq, hd;
+  long long total;      // sum over groups of rows * NQ * HD / 8
+  int g_b[kMaxSplitGroups], g_q0[kMaxSplitGroups], g_rows[kMaxSplitGroups];
+  int g_n[kMaxSplitGroups], g_part0[kMaxSplitGroups];
+  long long g_prefix[kMaxSplitGroups + 1];
+};
+
+__global__ void __launch_bounds__(256) splitkv_merge_kernel(const __grid_constant__ SplitMergeParams p) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const int per_head = p.hd / 8;
+  const int per_row = p.nq * per_head;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       idx < p.total; idx += stride) {
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.g_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+    }
+    const int g = lo;
+    const long long local = idx - p.g_prefix[g];
+    const int r = static_cast<int>(local / per_row);         // row within the block
+    const int rem = static_cast<int>(local - static_cast<long long>(r) * per_row);
+    const int h = rem / per_head;
+    const int part8 = rem - h * per_head;
+    const int n = p.g_n[g];
+    float m = -INFINITY;
+    for (int s = 0; s < n; ++s) {
+      const long long pr = static_cast<long long>(p.g_part0[g]) + static_cast<long long>(s) * p.g_rows[g] + r;
+      m = fmaxf(m, p.ws_lse[pr * p.nq + h]);
+    }
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.f;
+    for (int s = 0; s < n; ++s) {
+      const long long pr = static_cast<long long>(p.g_part0[g]) + static_cast<long long>(s) * p.g_rows[g] + r;
+      const float w = __expf(p.ws_lse[pr * p.nq + h] - m);
+      wsum += w;
+      const float* src = p.ws_o + (pr * p.nq + h) * p.hd + part8 * 8;
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 b = *reinterpret_cast<const float4*>(src + 4);
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+    const float inv = 1.f / wsum;
+    const long long tok = static_cast<long long>(p.g_b[g]) * p.C + p.g_q0[g] + r;
+    uint4 o;
+    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(p.out + (tok * p.nq + h) * p.hd + part8 * 8) = o;
+    if (part8 == 0 && p.lse != nullptr) p.lse[tok * p.nq + h] = m + __logf(wsum);
+  }
+}
+
 }  // namespace cpattn

@@ -1,0 +1,153 @@
+// Host-side work plan of one prefill launch.
+//
+// A row block is (sequence b, 128-row q block qb); its unit (one q head)
+// walks the virtual tile index v over n_cache cache tiles then the causal
+// current tiles 0..qb.  The plan lists work blocks, each a row block with a
+// slice [v0, v1) of that walk, longest first (a persistent grid takes them in
+// order, so the longest start first).
+//
+// Split-KV (for small chunks and decode): when a few long walks would leave
+// most SMs idle, a row block's walk is cut into pieces of about the average
+// work per SM.  Each piece writes fp32 O / l and its LSE for the block's
+// valid rows into a workspace ("partial rows"), and a merge pass combines
+// the pieces of each row by their LSE.  This is the single-GPU counterpart of
+// the pages' spilled running (m, l, acc) for very long contexts (PCP
+// ring-cache PR, Design section), with the walk cut across SMs instead of
+// across launches.
+#pragma once
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "cpattn.h"
+#include "merge.cuh"
+#include "walk.cuh"
+
+namespace cpattn {
+
+enum : int { kRegionAll = 0, kRegionCache = 1, kRegionCurrent = 2 };
+constexpr int kSplitOff = -1;   // never split
+constexpr int kSplitAuto = 0;   // split when the longest walk dominates
+constexpr int kMinPieceTiles = 16;
+constexpr int kMaxVirtualTiles = 65535;  // v0 and v1 are packed in 16 bits each
+
+struct WorkBlock {
+  int b, qb, v0, v1;
+  int part;  // -1: writes the output; else the first partial row of a piece
+};
+
+struct SplitGroup {
+  int b, q0, rows, n, part0;  // piece s has partial rows part0 + s * rows ..
+};
+
+struct WorkPlan {
+  std::vector<int> ncache;         // cache tiles per sequence
+  std::vector<WorkBlock> blocks;   // longest first
+  std::vector<SplitGroup> groups;  // row blocks cut into pieces
+  long long partial_rows = 0;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace bytes of a plan: fp32 O / l then the LSE, both 256-byte aligned.
+inline size_t plan_workspace_bytes(const WorkPlan& w, int nq, int hd) {
+  if (w.partial_rows == 0) return 0;
+  const size_t rows = static_cast<size_t>(w.partial_rows) * static_cast<size_t>(nq);
+  return align256(rows * static_cast<size_t>(hd) * 4) + align256(rows * 4);
+}
+
+// region: kRegionAll, or the two-launch variant's cache-only / current-only
+// halves (never split).  split: kSplitOff, kSplitAuto, or > 0 = cut every walk
+// longer than that many tiles into pieces of at most that many.  slots: the
+// number of SMs the persistent grid spans.  Returns false with `why` when the
+// plan exceeds the kernel's tables.
+inline bool make_plan(const cpattn_config& c, int num_seqs, const int32_t* cache_lens,
+                      const int32_t* chunk_lens, int region, int split, int slots,
+                      WorkPlan* plan, std::string* why) {
+  plan->ncache.assign(num_seqs, 0);
+  plan->blocks.clear();
+  plan->groups.clear();
+  plan->partial_rows = 0;
+  struct Row { int b, qb, v0, v1, rows; };
+  std::vector<Row> rows;
+  for (int b = 0; b < num_seqs; ++b) {
+    const int nc = cache_tile_count(cache_lens[b], c.num_shards, c.shard_capacity);
+    plan->ncache[b] = nc;
+    if (region == kRegionCache && nc == 0) continue;  // no cache-only work
+    const int nqb = (chunk_lens[b] + kBQ - 1) / kBQ;
+    for (int qb = 0; qb < nqb; ++qb) {
+      const int v0 = region == kRegionCurrent ? nc : 0;
+      const int v1 = region == kRegionCache ? nc : nc + qb + 1;
+      if (v1 > kMaxVirtualTiles) {
+        *why = "a cache walk longer than 65535 - q blocks tiles";
+        return false;
+      }
+      rows.push_back({b, qb, v0, v1, std::min(kBQ, chunk_lens[b] - qb * kBQ)});
+    }
+  }
+
+  // Which row blocks to cut, and into how many pieces.
+  std::vector<int> pieces(rows.size(), 1);
+  if (split != kSplitOff && region == kRegionAll && !rows.empty()) {
+    long long total = 0;
+    int longest = 0;
+    for (const Row& r : rows) {
+      total += static_cast<long long>(c.num_q_heads) * (r.v1 - r.v0);
+      longest = std::max(longest, r.v1 - r.v0);
+    }
+    const long long avg = (total + slots - 1) / std::max(slots, 1);
+    const int target = split > 0 ? split
+                                 : static_cast<int>(std::max<long long>(avg, kMinPieceTiles));
+    const bool worth = split > 0 || longest > target + target / 4;
+    if (worth) {
+      std::vector<int> order(rows.size());
+      for (size_t i = 0; i < rows.size(); ++i) order[i] = static_cast<int>(i);
+      std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        return rows[a].v1 - rows[a].v0 > rows[b].v1 - rows[b].v0;
+      });
+      size_t nblocks = rows.size();
+      int groups = 0;
+      for (int i : order) {
+        const int n = rows[i].v1 - rows[i].v0;
+        if (n <= target) break;
+        const int k = (n + target - 1) / target;
+        if (groups == kMaxSplitGroups || nblocks + k - 1 > CPATTN_MAX_ROW_BLOCKS) break;
+        pieces[i] = k;
+        nblocks += k - 1;
+        ++groups;
+      }
+    }
+  }
+
+  for (size_t i = 0; i < rows.size(); ++i) {
+    const Row& r = rows[i];
+    const int k = pieces[i];
+    if (k == 1) {
+      plan->blocks.push_back({r.b, r.qb, r.v0, r.v1, -1});
+      continue;
+    }
+    const int n = r.v1 - r.v0;
+    const int part0 = static_cast<int>(plan->partial_rows);
+    plan->groups.push_back({r.b, r.qb * kBQ, r.rows, k, part0});
+    for (int s = 0; s < k; ++s) {
+      const int a = r.v0 + static_cast<int>(static_cast<long long>(n) * s / k);
+      const int e = r.v0 + static_cast<int>(static_cast<long long>(n) * (s + 1) / k);
+      plan->blocks.push_back({r.b, r.qb, a, e, part0 + s * r.rows});
+    }
+    plan->partial_rows += static_cast<long long>(k) * r.rows;
+  }
+  if (plan->blocks.size() > CPATTN_MAX_ROW_BLOCKS) {
+    *why = "more than CPATTN_MAX_ROW_BLOCKS row blocks";
+    return false;
+  }
+  if (plan->partial_rows * c.num_q_heads >= (1LL << 31)) {
+    *why = "split-KV partial rows exceed the 32-bit index range";
+    return false;
+  }
+  std::stable_sort(plan->blocks.begin(), plan->blocks.end(),
+                   [](const WorkBlock& a, const WorkBlock& b) { return a.v1 - a.v0 > b.v1 - b.v0; });
+  return true;
+}
+
+}  // namespace cpattn

@@ -57,13 +57,21 @@ struct PrefillParams {
   int* status;
   unsigned long long timeout_ns;
   int num_units, nq, nkv, group, P, S, C, debug_flags;
-  // Region restriction (the two-launch variant): 0 both regions in one
-  // softmax, 1 cache tiles only, 2 current tiles only.  out_f32: O is written
-  // as fp32 (partial results for the LSE merge) instead of bf16.
-  int region, out_f32;
+  // out_f32: O is written to `out` as fp32 (the two-launch variant's partial
+  // results) instead of bf16.
+  int out_f32;
   float scale_log2;
+  float* ws_o;    // split-KV pieces: fp32 O / l, [partial rows][NQ][HD]
+  float* ws_lse;  // split-KV pieces: LSE, [partial rows][NQ]
   SeqInfo seqs[CPATTN_MAX_SEQS];
-  uint32_t blocks[CPATTN_MAX_ROW_BLOCKS];  // (b << 16) | q block, longest first
+  // Work blocks, longest first.  blocks[i] = (b << 16) | q block;
+  // range[i] = (v0 << 16) | v1: the slice [v0, v1) of the block's virtual tile
+  // walk (its n_cache cache tiles, then its causal current tiles 0..qb);
+  // part[i] = -1 when the block writes the final output, else the first
+  // partial row of a split-KV piece (rows q0.. of the block follow it).
+  uint32_t blocks[CPATTN_MAX_ROW_BLOCKS];
+  uint32_t range[CPATTN_MAX_ROW_BLOCKS];
+  int part[CPATTN_MAX_ROW_BLOCKS];
 };
 
 enum : int { kDebugDropArrive = 1 };
@@ -118,8 +126,12 @@ struct Layout {
   static_assert(HD + 2 * kBKV <= TMEM_COLS, "TMEM budget");
 };
 
+static_assert(sizeof(PrefillParams) <= 32764, "kernel parameter budget");
+
 struct Unit {
-  int b, h, g, qb, q0, L, c, n_cache, n_tiles;
+  int b, h, g, qb, q0, L, c, n_cache;
+  int v0, n_tiles;  // this work block's tiles: virtual indices [v0, v0 + n_tiles)
+  int part;         // -1, or the first partial row of a split-KV piece
 };
 
 __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
@@ -133,8 +145,11 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
   U.q0 = U.qb * kBQ;
   U.L = p.seqs[U.b].cache_len;
   U.c = p.seqs[U.b].chunk_len;
-  U.n_cache = p.region == 2 ? 0 : p.seqs[U.b].n_cache_tiles;
-  U.n_tiles = U.n_cache + (p.region == 1 ? 0 : U.qb + 1);
+  U.n_cache = p.seqs[U.b].n_cache_tiles;
+  const uint32_t rg = p.range[blk];
+  U.v0 = static_cast<int>(rg >> 16);
+  U.n_tiles = static_cast<int>(rg & 0xFFFFu) - U.v0;
+  U.part = p.part[blk];
   return U;
 }
 
@@ -245,10 +260,15 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
         if (!load_sub(false, m, m, 0, y, z + j * Ly::VROWS)) return false;
       return true;
     };
+    // This block's slice of the walk starts at virtual tile U.v0.
+    const int skip = U.v0 < U.n_cache ? U.v0 : U.n_cache;
+    wk.skip(skip);
+    wv.skip(skip);
     // Same order as the MMA consumes them: K0, (K1, V0), (K2, V1), ..., V_last.
-    ok = load_k(0);
-    for (int v = 1; ok && v < U.n_tiles; ++v) ok = load_k(v) && load_v(v - 1);
-    if (ok) ok = load_v(U.n_tiles - 1);
+    const int v0 = U.v0, v1 = U.v0 + U.n_tiles;
+    ok = load_k(v0);
+    for (int v = v0 + 1; ok && v < v1; ++v) ok = load_k(v) && load_v(v - 1);
+    if (ok) ok = load_v(v1 - 1);
   }
 
   if (!ok) {
@@ -413,12 +433,14 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
     const Unit U = decode_unit(p, u);
     CacheWalk walk;
     walk.init(U.L, p.P, p.S);
+    walk.skip(U.v0 < U.n_cache ? U.v0 : U.n_cache);
     float m = -INFINITY;  // running reference max of the scaled logits (log2 units), per row
     float l = 0.f;        // this group's running sum of 2^(x - m)
     bool ok = true;
     bool left_at_vote = false;  // the only way out of the tile loop before its end
 
     for (int v = 0; v < U.n_tiles; ++v) {
+      const int va = U.v0 + v;  // virtual tile index within the unit's whole walk
       const uint32_t sb = tile_ctr & 1u;
       ok = wait(bar(Ly::B_SFULL + sb), (tile_ctr >> 1) & 1u, kSiteSFull);
       ok = __all_sync(0xFFFFFFFFu, ok);
@@ -427,7 +449,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       const uint32_t s_tmem = lane_tmem + HD + sb * kBKV + CW * h;
 
       // Region by value: one scalar picks the validity words of the tile.
-      const bool in_cache = v < U.n_cache;
+      const bool in_cache = va < U.n_cache;
       uint32_t mw[4];
       if (in_cache) {
         const int tile = walk.next();
@@ -437,7 +459,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
           walk.column_mask(tile, mw);
         }
       } else {
-        const int lim = (v - U.n_cache == U.qb) ? r + 1 : kBKV;
+        const int lim = (va - U.n_cache == U.qb) ? r + 1 : kBKV;
 #pragma unroll
         for (int q = 0; q < 4; ++q) mw[q] = causal_word(lim, q);
       }
@@ -608,15 +630,21 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
     const int row = U.q0 + r;
     const bool valid = row < U.c;
     const float inv_l = 1.f / l_row;
+    // A split-KV piece writes fp32 O / l and its LSE to its partial rows; a
+    // whole unit writes the output row (bf16, or fp32 when out_f32).
+    const bool partial = U.part >= 0;
     const long long tok = static_cast<long long>(U.b) * p.C + row;
-    uint4* orow = reinterpret_cast<uint4*>(p.out + (tok * p.nq + U.h) * HD + h * OCOLS);
-    float4* orow32 = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
-                                               (tok * p.nq + U.h) * HD + h * OCOLS);
+    const long long orow_i = (partial ? static_cast<long long>(U.part + r) : tok) * p.nq + U.h;
+    const bool f32 = partial || p.out_f32 != 0;
+    float* lse_out = partial ? p.ws_lse : p.lse;
+    uint4* orow = reinterpret_cast<uint4*>(p.out + orow_i * HD + h * OCOLS);
+    float4* orow32 = reinterpret_cast<float4*>((partial ? p.ws_o : reinterpret_cast<float*>(p.out)) +
+                                               orow_i * HD + h * OCOLS);
 #pragma unroll 1
     for (int ch = 0; ch < OCOLS / 32; ++ch) {
       uint32_t o[32];
       tmem_ld32_wait(lane_tmem + h * OCOLS + 32 * ch, o);
-      if (valid && p.out_f32) {
+      if (valid && f32) {
 #pragma unroll
         for (int v4 = 0; v4 < 8; ++v4)
           orow32[ch * 8 + v4] = make_float4(
@@ -634,8 +662,8 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
         }
       }
     }
-    if (h == 0 && valid && p.lse != nullptr)
-      p.lse[tok * p.nq + U.h] = (m + __log2f(l_row)) * 0.69314718055994531f;
+    if (h == 0 && valid && lse_out != nullptr)
+      lse_out[orow_i] = (m + __log2f(l_row)) * 0.69314718055994531f;
     tc_fence_before();
   }
 }

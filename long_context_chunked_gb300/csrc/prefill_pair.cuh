@@ -132,10 +132,15 @@ __device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint
       }
       return true;
     };
+    // This block's slice of the walk starts at virtual tile U.v0.
+    const int skip = U.v0 < U.n_cache ? U.v0 : U.n_cache;
+    wk.skip(skip);
+    wv.skip(skip);
     // Same order as the MMA consumes them: K0, (K1, V0), (K2, V1), ..., V_last.
-    ok = load_k(0);
-    for (int v = 1; ok && v < U.n_tiles; ++v) ok = load_k(v) && load_v(v - 1);
-    if (ok) ok = load_v(U.n_tiles - 1);
+    const int v0 = U.v0, v1 = U.v0 + U.n_tiles;
+    ok = load_k(v0);
+    for (int v = v0 + 1; ok && v < v1; ++v) ok = load_k(v) && load_v(v - 1);
+    if (ok) ok = load_v(v1 - 1);
   }
 
   if (!ok && rank == 0) {

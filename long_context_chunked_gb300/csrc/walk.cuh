@@ -64,6 +64,22 @@ struct CacheWalk {
 
   __host__ __device__ __forceinline__ bool done() const { return s >= P; }
 
+  // Skip the next n tiles of the walk (a work item that starts mid-walk):
+  // whole shard ranges at a time, O(P).  Skipping past the end finishes it.
+  __host__ __device__ __forceinline__ void skip(int n) {
+    while (n > 0 && !done()) {
+      const int left = k_last - k + 1;  // tiles still to emit in shard s's range
+      if (n < left) {
+        k += n;
+        prev_last = k - 1;
+        return;
+      }
+      n -= left;
+      prev_last = k_last;
+      next_shard();
+    }
+  }
+
   // Emit the current tile index and advance.  Interior tiles of a shard's
   // range are wholly valid (last_full); only the tiles at its edges need the
   // column mask.

@@ -133,3 +133,79 @@ def test_cache_walk_tile_count_is_minimal_for_aligned_shards(lib):
     ctx = cp.Context(32, 2, 256, 8, 4096, 4096)
     tiles, masks = ctx.cache_walk(28672)
     assert len(tiles) == 224 and np.all(masks == 0xFFFFFFFF)
+
+
+# ---------------------------------------------------------------- split-KV
+@pytest.mark.parametrize("L,P,S", [(1000, 4, 300), (5000, 8, 700), (777, 8, 100), (129, 2, 65),
+                                   (40000, 8, 5003), (3, 8, 1)])
+def test_cache_walk_from_equals_the_tail_of_the_walk(lib, L, P, S):
+    """A split-KV piece starting at virtual tile `first` skips whole shard
+    ranges; it must visit exactly the rest of the full walk, same masks."""
+    ctx = cp.Context(2, 1, 128, P, S, 16)
+    tiles, masks = ctx.cache_walk(L)
+    for first in sorted({0, 1, 2, len(tiles) // 3, len(tiles) // 2, len(tiles) - 1, len(tiles),
+                         len(tiles) + 5}):
+        t2, m2 = ctx.cache_walk(L, first)
+        assert np.array_equal(t2, tiles[first:]), first
+        assert np.array_equal(m2, masks[first:]), first
+
+
+def _expected_split(ctx, cache_lens, chunk_lens, nq, hd, t):
+    """Pieces and workspace of a forced split at most t tiles long, from the
+    cache walk's tile counts: a walk of n > t tiles becomes ceil(n / t) pieces,
+    each writing the block's valid rows."""
+    blocks, rows = 0, 0
+    for L, c in zip(cache_lens, chunk_lens):
+        nc = len(ctx.cache_walk(L)[0])
+        for qb in range(-(-c // 128)):
+            n = nc + qb + 1
+            k = -(-n // t) if n > t else 1
+            blocks += k
+            if k > 1:
+                rows += k * min(128, c - 128 * qb)
+    a256 = lambda x: (x + 255) // 256 * 256
+    ws = a256(rows * nq * hd * 4) + a256(rows * nq * 4) if rows else 0
+    return ws, blocks
+
+
+@pytest.mark.parametrize("t", [1, 3, 16, 1000])
+def test_splitkv_forced_plan_sizes(lib, t):
+    ctx = cp.Context(8, 2, 128, 4, 4000, 384)
+    cl, ch = [0, 1000, 129, 12000], [300, 1, 384, 77]
+    ws, blocks = ctx.splitkv_workspace(cl, ch, t)
+    assert (ws, blocks) == _expected_split(ctx, cl, ch, 8, 128, t)
+
+
+def test_splitkv_automatic_policy(lib):
+    """Automatic: a prefill-sized batch is never split; a decode step against
+    a long cache is cut into about one piece per SM's share."""
+    ctx = cp.Context(32, 2, 256, 8, 16400, 4096)
+    ws, blocks = ctx.splitkv_workspace([126976], [4096], 0)
+    assert ws == 0 and blocks == 32
+    ws, blocks = ctx.splitkv_workspace([126976], [1], 0)
+    assert ws > 0 and 1 < blocks <= 64
+    # Pieces of a decode row hold 1 row x NQ heads x (HD + 1) floats each.
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert ws == a256(blocks * 32 * 256 * 4) + a256(blocks * 32 * 4)
+
+
+def test_splitkv_registration_checks(lib):
+    ctx = cp.Context(8, 2, 128, 2, 64, 32)
+    with pytest.raises(cp.CpattnError) as e:
+        ctx.set_splitkv(None, -1)
+    assert e.value.status == cp.E_INVALID
+    st = ctx.lib.cpattn_set_splitkv(ctx._h, 256 + 16, 1 << 20, 0)  # not 256-byte aligned
+    assert st == cp.E_INVALID
+    assert ctx.lib.cpattn_set_splitkv(ctx._h, 4096, 1 << 20, 0) == cp.OK
+    assert ctx.lib.cpattn_set_splitkv(ctx._h, None, 0, 0) == cp.OK  # off again
+
+
+def test_splitkv_workspace_too_small_is_refused_before_launch(lib):
+    ctx = cp.Context(8, 2, 128, 4, 4000, 64)
+    cl, ch = [12000], [5]
+    need, _ = ctx.splitkv_workspace(cl, ch, 4)
+    assert need > 0
+    assert ctx.lib.cpattn_set_splitkv(ctx._h, 4096, need - 256, 4) == cp.OK
+    A = 256
+    st = ctx.prefill_raw(cl, ch, A, A, A, A, A, A, None, stream=0)
+    assert st == cp.E_INVALID and "split-KV workspace" in ctx.last_error()
