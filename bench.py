@@ -419,6 +419,86 @@ def run_cumulative(contexts, fast_p=False, seed=7):
         del kc, vc, ctx
 
 
+# Small-chunk and decode workloads for split-KV (NQ=32, NKV=2, HD=256, P=8,
+# the pages' model shape): (name, cache lengths, chunk lengths).
+SPLITKV_CASES = [
+    ("decode_1x128k", [126976], [1]),
+    ("decode_8x32k", [32768] * 8, [1] * 8),
+    ("chunk37_15k", [15000], [37]),
+    ("chunk128_4x64k", [65536] * 4, [128] * 4),
+]
+
+
+def run_splitkv(fast_p=False, reps=20, seed=11):
+    """Each small-chunk workload fused (one launch) and split-KV (automatic
+    plan: pieces + merge; the same single launch when the plan cuts nothing),
+    alternating rep by rep, L2 flushed before every rep, CUDA events on the
+    launching stream.  Prints one JSON line per workload with both times, the
+    plan's work blocks, and the split time against the HBM roofline of its
+    algorithmic bytes (the K/V prefix read once, Q, O)."""
+    import torch
+    import long_context_chunked_gb300 as cp
+    dev = torch.device("cuda", 0)
+    NQ, NKV, HD, P = 32, 2, 256, 8
+    peaks, peak_kind = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    gen = torch.Generator().manual_seed(seed)
+    for name, cl, ch in SPLITKV_CASES:
+        B, C = len(cl), max(max(ch), 1)
+        S = (max(l + c for l, c in zip(cl, ch)) + P - 1) // P
+        q = torch.randn(B * C, NQ, HD, generator=gen).to(torch.bfloat16).to(dev)
+        kn = torch.randn(B * C, NKV, HD, generator=gen).to(torch.bfloat16).to(dev)
+        vn = torch.randn(B * C, NKV, HD, generator=gen).to(torch.bfloat16).to(dev)
+        kc = torch.randn(B, NKV, P, S, HD, generator=gen).to(torch.bfloat16).to(dev)
+        vc = torch.randn(B, NKV, P, S, HD, generator=gen).to(torch.bfloat16).to(dev)
+        out = torch.empty_like(q)
+        ctx = cp.Context(NQ, NKV, HD, P, S, C, 0.0, fast_p)
+        need, blocks = ctx.splitkv_workspace(cl, ch, 0)
+        ws = torch.empty(max(need // 4, 64), dtype=torch.float32, device=dev)
+
+        def one(split):
+            ctx.set_splitkv(ws if split else None, 0)
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ctx.prefill(cl, ch, q, kn, vn, kc, vc, out)
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+
+        for _ in range(3):  # warm-up, both arms
+            one(False)
+            one(True)
+        # The two arms alternate rep by rep, so clock or power drift during the
+        # run affects both alike.
+        fused, split = [], []
+        for _ in range(reps):
+            fused.append(one(False))
+            split.append(one(True))
+        if ctx.sync_status() != 0:
+            raise RuntimeError(ctx.last_error())
+        fused_ms, split_ms = statistics.median(fused), statistics.median(split)
+        flops = sum(4 * HD * NQ * (c * l + c * (c + 1) // 2) for l, c in zip(cl, ch))
+        kv_bytes = sum(2 * NKV * HD * 2 * (l + c) for l, c in zip(cl, ch))
+        io_bytes = sum(c for c in ch) * NQ * HD * 2 * 2
+        gbs = (kv_bytes + io_bytes) / (split_ms * 1e-3) / 1e9
+        print(json.dumps({
+            "mode": "splitkv", "workload": name, "cache_lens": cl, "chunk_lens": ch,
+            "precision": "fast_p" if fast_p else "accurate P",
+            "row_blocks": sum(-(-c // 128) for c in ch), "work_blocks_split": blocks,
+            "fused_ms": round(fused_ms, 4), "split_ms": round(split_ms, 4),
+            "speedup": round(fused_ms / split_ms, 2),
+            "split_tflops": round(flops / (split_ms * 1e-3) / 1e12, 2),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": round(gbs / float(peaks["hbm_gbs"]), 4),
+                         "peak_kind": f"HBM copy, {peak_kind}",
+                         "bytes": "K/V prefix and chunk read once + Q + O"},
+            "l2": "flushed before every rep"}), flush=True)
+        del q, kn, vn, kc, vc, out, ws, ctx
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,11 +512,16 @@ def main():
                     help="two_launch: the PR's removed variant (cache-only + current-only "
                          "launches + LSE merge), to measure what fusion saves")
     ap.add_argument("--ref-rows", type=int, default=384)
+    ap.add_argument("--splitkv", action="store_true",
+                    help="small-chunk and decode workloads, fused vs split-KV")
     ap.add_argument("--cumulative", default=None,
                     help="comma-separated request lengths (e.g. 8k,32k,1M): per-request "
                          "cumulative prefill instead of the step benchmark")
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.splitkv:
+        run_splitkv(fast_p=args.fast_p)
+        return
     if args.cumulative:
         mult = {"k": 1024, "m": 1024 * 1024}
         ns = [int(x[:-1]) * mult[x[-1].lower()] if x[-1].lower() in mult else int(x)

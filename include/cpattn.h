@@ -172,11 +172,14 @@ cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
  *                    share one workspace.
  *   workspace_bytes  its size; a prefill whose plan needs more fails with
  *                    E_INVALID (query the need with cpattn_splitkv_workspace)
- *   max_split_tiles  0: automatic -- walks are cut only when the longest one
- *                    exceeds 1.25x the average work per SM, into pieces of
- *                    about that average (at least 16 tiles); > 0: every walk
- *                    longer than this many tiles is cut into pieces of at
- *                    most this many (for tests and tuning)
+ *   max_split_tiles  0: automatic -- a cost model of the persistent grid
+ *                    (units handed out cyclically, longest first, each
+ *                    costing its tiles plus a fixed fill/drain) picks, among
+ *                    pieces of ceil(n_max / k) tiles (k = 2..64, at least 16
+ *                    tiles), the cut with the lowest modelled makespan, and
+ *                    cuts only if that beats the unsplit plan by 10 %;
+ *                    > 0: every walk longer than this many tiles is cut into
+ *                    pieces of at most this many (for tests and tuning)
  * Limits: at most 256 row blocks are cut per call (the longest ones), and
  * the pieces count against CPATTN_MAX_ROW_BLOCKS.
  * Errors: E_INVALID (NULL ctx, max_split_tiles < 0, misaligned workspace).

@@ -178,9 +178,15 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
   return after_launch(ctx, stream, "prefill launch");
 }
 
-// SMs the persistent grid spans (the plan's notion of parallel slots; with
-// CTA pairs both the units and the slots halve, so the ratio is the same).
-int plan_slots(const cpattn_ctx* ctx) { return ctx->num_sms > 0 ? ctx->num_sms : 148; }
+// The plan's executors and units per work block: SM pairs and q-head pairs
+// when the prefill runs as CTA pairs, else SMs and q heads (148 SMs when no
+// device is present, for host-side planning).
+void plan_shape(const cpattn_ctx* ctx, int* executors, int* units_per_block) {
+  const int sms = ctx->num_sms > 0 ? ctx->num_sms : 148;
+  const bool paired = ctx->pair_mode != 0 && (ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads) % 2 == 0;
+  *executors = paired ? sms / 2 : sms;
+  *units_per_block = paired ? ctx->cfg.num_q_heads / 2 : ctx->cfg.num_q_heads;
+}
 
 cpattn_status dispatch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st) {
   const int HD = ctx->cfg.head_dim;
@@ -251,8 +257,10 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
   static thread_local cpattn::WorkPlan plan;
   std::string why;
-  if (!cpattn::make_plan(c, num_seqs, cache_lens, chunk_lens, region, split, plan_slots(ctx),
-                         &plan, &why))
+  int executors = 0, units_per_block = 0;
+  plan_shape(ctx, &executors, &units_per_block);
+  if (!cpattn::make_plan(c, num_seqs, cache_lens, chunk_lens, region, split, executors,
+                         units_per_block, &plan, &why))
     return fail(ctx, CPATTN_E_UNSUPPORTED, why);
   if (plan.blocks.empty()) return CPATTN_OK;
   const size_t ws_need = cpattn::plan_workspace_bytes(plan, NQ, HD);
@@ -519,8 +527,10 @@ cpattn_status cpattn_splitkv_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
   if (s != CPATTN_OK) return s;
   cpattn::WorkPlan plan;
   std::string why;
+  int executors = 0, units_per_block = 0;
+  plan_shape(ctx, &executors, &units_per_block);
   if (!cpattn::make_plan(ctx->cfg, num_seqs, cache_lens, chunk_lens, cpattn::kRegionAll,
-                         max_split_tiles, plan_slots(ctx), &plan, &why))
+                         max_split_tiles, executors, units_per_block, &plan, &why))
     return CPATTN_E_UNSUPPORTED;
   *bytes = cpattn::plan_workspace_bytes(plan, ctx->cfg.num_q_heads, ctx->cfg.head_dim);
   if (work_blocks != nullptr) *work_blocks = static_cast<int32_t>(plan.blocks.size());

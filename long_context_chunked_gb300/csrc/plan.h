@@ -7,8 +7,8 @@
 // order, so the longest start first).
 //
 // Split-KV (for small chunks and decode): when a few long walks would leave
-// most SMs idle, a row block's walk is cut into pieces of about the average
-// work per SM.  Each piece writes fp32 O / l and its LSE for the block's
+// most SMs idle, a row block's walk is cut into pieces (their length chosen
+// by a cost model of the grid's rounds, below).  Each piece writes fp32 O / l and its LSE for the block's
 // valid rows into a workspace ("partial rows"), and a merge pass combines
 // the pieces of each row by their LSE.  This is the single-GPU counterpart of
 // the pages' spilled running (m, l, acc) for very long contexts (PCP
@@ -28,8 +28,33 @@ namespace cpattn {
 
 enum : int { kRegionAll = 0, kRegionCache = 1, kRegionCurrent = 2 };
 constexpr int kSplitOff = -1;   // never split
-constexpr int kSplitAuto = 0;   // split when the longest walk dominates
+constexpr int kSplitAuto = 0;   // split when the cost model says it pays
 constexpr int kMinPieceTiles = 16;
+constexpr int kUnitOverheadTiles = 2;  // pipeline fill and drain of one unit, in tile times
+constexpr int kMaxPieceCandidates = 64;
+// Costs of a piece beyond its tiles, in tile times (a tile takes ~1.5 us per
+// SM or SM pair): writing its fp32 partial rows (~64 KB per SM per tile
+// time), and the merge pass reading all partials back (~10 MB GPU-wide per
+// tile time).  Measured: without them the model cut 128-row blocks into
+// pieces that then ran 5 % slower than the fused walk.
+constexpr long long kPieceWriteBytesPerTile = 64 << 10;
+constexpr long long kMergeBytesPerTile = 10 << 20;
+
+// Cost model of a plan: the persistent grid hands units out cyclically in list
+// order -- executor e runs units e, e + E, e + 2E, ... -- and a unit costs its
+// tiles plus a fixed fill/drain overhead.  `lens` holds one entry per work
+// block, longest first (any per-unit extra cost already added); each block
+// has units_per_block units.  With the list sorted, executor 0 takes the
+// longest unit of every round and has the most rounds, so its load is the
+// makespan: O(rounds), no per-executor state.
+inline long long cyclic_makespan(const std::vector<int>& lens, int units_per_block,
+                                 int executors) {
+  const long long total = static_cast<long long>(lens.size()) * units_per_block;
+  const long long E = std::max(executors, 1);
+  long long m = 0;
+  for (long long i = 0; i < total; i += E) m += lens[static_cast<size_t>(i / units_per_block)] + kUnitOverheadTiles;
+  return m;
+}
 constexpr int kMaxVirtualTiles = 65535;  // v0 and v1 are packed in 16 bits each
 
 struct WorkBlock {
@@ -59,12 +84,13 @@ inline size_t plan_workspace_bytes(const WorkPlan& w, int nq, int hd) {
 
 // region: kRegionAll, or the two-launch variant's cache-only / current-only
 // halves (never split).  split: kSplitOff, kSplitAuto, or > 0 = cut every walk
-// longer than that many tiles into pieces of at most that many.  slots: the
-// number of SMs the persistent grid spans.  Returns false with `why` when the
-// plan exceeds the kernel's tables.
+// longer than that many tiles into pieces of at most that many.  executors:
+// how many units run at once (SMs, or SM pairs); units_per_block: units one
+// work block gives them (q heads, or q-head pairs).  Returns false with `why`
+// when the plan exceeds the kernel's tables.
 inline bool make_plan(const cpattn_config& c, int num_seqs, const int32_t* cache_lens,
-                      const int32_t* chunk_lens, int region, int split, int slots,
-                      WorkPlan* plan, std::string* why) {
+                      const int32_t* chunk_lens, int region, int split, int executors,
+                      int units_per_block, WorkPlan* plan, std::string* why) {
   plan->ncache.assign(num_seqs, 0);
   plan->blocks.clear();
   plan->groups.clear();
@@ -87,35 +113,86 @@ inline bool make_plan(const cpattn_config& c, int num_seqs, const int32_t* cache
     }
   }
 
-  // Which row blocks to cut, and into how many pieces.
+  // Which row blocks to cut, and into how many pieces.  Pieces of at most
+  // `target` tiles; the automatic policy tries the targets ceil(n_max / k) and
+  // keeps the one whose modelled makespan is lowest, if it beats the unsplit
+  // plan by 10 %.
   std::vector<int> pieces(rows.size(), 1);
-  if (split != kSplitOff && region == kRegionAll && !rows.empty()) {
-    long long total = 0;
-    int longest = 0;
-    for (const Row& r : rows) {
-      total += static_cast<long long>(c.num_q_heads) * (r.v1 - r.v0);
-      longest = std::max(longest, r.v1 - r.v0);
+  std::vector<int> order(rows.size());  // row blocks, longest walk first
+  for (size_t i = 0; i < rows.size(); ++i) order[i] = static_cast<int>(i);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    return rows[a].v1 - rows[a].v0 > rows[b].v1 - rows[b].v0;
+  });
+  auto cut = [&](int target, std::vector<int>* out) {
+    out->assign(rows.size(), 1);
+    size_t nblocks = rows.size();
+    int groups = 0;
+    for (int i : order) {
+      const int n = rows[i].v1 - rows[i].v0;
+      if (n <= target) break;
+      const int k = (n + target - 1) / target;
+      if (groups == kMaxSplitGroups || nblocks + k - 1 > CPATTN_MAX_ROW_BLOCKS) break;
+      (*out)[i] = k;
+      nblocks += k - 1;
+      ++groups;
     }
-    const long long avg = (total + slots - 1) / std::max(slots, 1);
-    const int target = split > 0 ? split
-                                 : static_cast<int>(std::max<long long>(avg, kMinPieceTiles));
-    const bool worth = split > 0 || longest > target + target / 4;
-    if (worth) {
-      std::vector<int> order(rows.size());
-      for (size_t i = 0; i < rows.size(); ++i) order[i] = static_cast<int>(i);
-      std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
-        return rows[a].v1 - rows[a].v0 > rows[b].v1 - rows[b].v0;
-      });
-      size_t nblocks = rows.size();
-      int groups = 0;
-      for (int i : order) {
-        const int n = rows[i].v1 - rows[i].v0;
-        if (n <= target) break;
-        const int k = (n + target - 1) / target;
-        if (groups == kMaxSplitGroups || nblocks + k - 1 > CPATTN_MAX_ROW_BLOCKS) break;
-        pieces[i] = k;
-        nblocks += k - 1;
-        ++groups;
+  };
+  const int heads_per_unit = c.num_q_heads / std::max(units_per_block, 1);
+  std::vector<int> lens;
+  lens.reserve(rows.size() * 4);
+  auto makespan = [&](const std::vector<int>& k) {
+    lens.clear();
+    long long merge_bytes = 0;
+    for (size_t i = 0; i < rows.size(); ++i) {
+      const int n = rows[i].v1 - rows[i].v0;
+      // A piece also writes rows x heads x HD fp32 partials.
+      const long long wbytes =
+          static_cast<long long>(rows[i].rows) * heads_per_unit * c.head_dim * 4;
+      const int extra = k[i] > 1 ? static_cast<int>((wbytes + kPieceWriteBytesPerTile - 1) /
+                                                    kPieceWriteBytesPerTile)
+                                 : 0;
+      if (k[i] > 1)
+        merge_bytes += static_cast<long long>(k[i]) * rows[i].rows * c.num_q_heads *
+                       (c.head_dim + 1) * 4;
+      for (int s = 0; s < k[i]; ++s)
+        lens.push_back(static_cast<int>(static_cast<long long>(n) * (s + 1) / k[i] -
+                                        static_cast<long long>(n) * s / k[i]) + extra);
+    }
+    std::sort(lens.begin(), lens.end(), [](int a, int b) { return a > b; });
+    return cyclic_makespan(lens, units_per_block, executors) +
+           (merge_bytes + kMergeBytesPerTile - 1) / kMergeBytesPerTile;
+  };
+  if (split != kSplitOff && region == kRegionAll && !rows.empty()) {
+    if (split > 0) {
+      cut(split, &pieces);
+    } else {
+      int n_max = 0;
+      long long total = 0;
+      for (const Row& r : rows) {
+        n_max = std::max(n_max, r.v1 - r.v0);
+        total += static_cast<long long>(units_per_block) * (r.v1 - r.v0 + kUnitOverheadTiles);
+      }
+      const long long ideal = (total + executors - 1) / std::max(executors, 1);
+      const long long base = makespan(pieces);
+      if (base * 10 > ideal * 11) {  // rounds of the grid leave more than 10 % idle
+        long long best = base;
+        std::vector<int> trial;
+        // k = 2..8, then a geometric ladder to 64: the makespan moves in
+        // steps of whole grid rounds, so finer k rarely matters.
+        static const int kLadder[] = {2, 3, 4, 5, 6, 7, 8, 10, 12, 14, 16, 20, 24, 28, 32,
+                                      40, 48, 56, 64};
+        for (int k : kLadder) {
+          if (k > kMaxPieceCandidates) break;
+          const int target = (n_max + k - 1) / k;
+          if (target < kMinPieceTiles) break;
+          cut(target, &trial);
+          const long long m = makespan(trial);
+          if (m < best) {
+            best = m;
+            pieces = trial;
+          }
+        }
+        if (best * 10 > base * 9) pieces.assign(rows.size(), 1);  // under 10 %: not worth it
       }
     }
   }

@@ -122,14 +122,16 @@ struct CacheWalk {
   }
 };
 
-// Number of cache tiles the walk visits for cache length L.
+// Number of cache tiles the walk visits for cache length L: whole shard
+// ranges at a time (as skip() moves), O(P).
 __host__ __device__ inline int cache_tile_count(int L, int P, int S) {
   CacheWalk w;
   w.init(L, P, S);
   int n = 0;
   while (!w.done()) {
-    w.next();
-    ++n;
+    n += w.k_last - w.k + 1;
+    w.prev_last = w.k_last;
+    w.next_shard();
   }
   return n;
 }
