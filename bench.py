@@ -183,6 +183,8 @@ class DeviceState:
 
     def write_kv(self, stream=None):
         w = self.w
+        if self.variant == "fused_write":  # the write happens inside prefill()
+            return
         self.ctx.write_kv(w.cache_lens, w.chunk_lens, self.k_new, self.v_new, self.k_cache,
                           self.v_cache, stream)
 
@@ -192,6 +194,11 @@ class DeviceState:
             self.ctx.prefill_two_launch(w.cache_lens, w.chunk_lens, self.q, self.k_new,
                                         self.v_new, self.k_cache, self.v_cache, self.out,
                                         self.workspace, None, stream)
+            return
+        if self.variant == "fused_write":
+            self.ctx.prefill_write_kv(w.cache_lens, w.chunk_lens, self.q, self.k_new,
+                                      self.v_new, self.k_cache, self.v_cache, self.out, None,
+                                      stream)
             return
         self.ctx.prefill(w.cache_lens, w.chunk_lens, self.q, self.k_new, self.v_new,
                          self.k_cache, self.v_cache, self.out, None, stream)
@@ -263,8 +270,13 @@ def time_e2e(st: DeviceState, steps: int, warmup: int):
             up.record(cs)
         ks.wait_event(up)
         ks.wait_event(output_free[s])
-        st.ctx.write_kv(w.cache_lens, w.chunk_lens, b["k"], b["v"], st.k_cache, st.v_cache, ks)
-        if st.variant == "two_launch":
+        if st.variant != "fused_write":
+            st.ctx.write_kv(w.cache_lens, w.chunk_lens, b["k"], b["v"], st.k_cache, st.v_cache,
+                            ks)
+        if st.variant == "fused_write":
+            st.ctx.prefill_write_kv(w.cache_lens, w.chunk_lens, b["q"], b["k"], b["v"],
+                                    st.k_cache, st.v_cache, b["o"], None, ks)
+        elif st.variant == "two_launch":
             st.ctx.prefill_two_launch(w.cache_lens, w.chunk_lens, b["q"], b["k"], b["v"],
                                       st.k_cache, st.v_cache, b["o"], st.workspace, None, ks)
         else:
@@ -508,8 +520,9 @@ def main():
     ap.add_argument("--config", default="32k", choices=sorted(BY_NAME))
     ap.add_argument("--fast-p", action="store_true", help="P rounded once to bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--variant", default="fused", choices=["fused", "two_launch"],
-                    help="two_launch: the PR's removed variant (cache-only + current-only "
+    ap.add_argument("--variant", default="fused", choices=["fused", "two_launch", "fused_write"],
+                    help="fused_write: the KV write inside the prefill launch; "
+                         "two_launch: the PR's removed variant (cache-only + current-only "
                          "launches + LSE merge), to measure what fusion saves")
     ap.add_argument("--ref-rows", type=int, default=384)
     ap.add_argument("--splitkv", action="store_true",
@@ -587,7 +600,7 @@ def main():
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "pinned host buffers; copies on a second stream overlap the previous/next step"},
-        "gpu_launches": (2 if args.variant == "fused" else 4) * args.steps,
+        "gpu_launches": {"fused": 2, "two_launch": 4, "fused_write": 1}[args.variant] * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

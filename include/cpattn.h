@@ -133,6 +133,25 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
                              void* out, float* lse, void* stream);
 
 /*
+ * cpattn_prefill and cpattn_write_kv of the same chunk in ONE launch (the
+ * KV write fused into the prefill kernel).  Idle lanes of each CTA's load
+ * warp copy the chunk's valid K/V rows into the striped caches while the
+ * prefill runs.  The copy is the same bit copy as cpattn_write_kv: every
+ * (token, kv head) once, pad rows and every other cache row untouched.  It
+ * cannot race the prefill: it writes only rows of tokens >= L_b, which the
+ * prefill never reads as keys.  Cache tiles at a shard's edge may load those
+ * rows as masked columns, and they hold finite values before and after.
+ * Arguments, layouts and errors are those of cpattn_prefill, with k_cache
+ * and v_cache also written (in place); a registered split-KV workspace is
+ * used as by cpattn_prefill.
+ */
+cpattn_status cpattn_prefill_write_kv(cpattn_ctx* ctx, int32_t num_seqs,
+                                      const int32_t* cache_lens, const int32_t* chunk_lens,
+                                      const void* q, const void* k_new, const void* v_new,
+                                      void* k_cache, void* v_cache, void* out, float* lse,
+                                      void* stream);
+
+/*
  * The two-launch variant the PR removed (Summary section: a cache-only launch
  * plus an LSE merge, strictly slower than the fused kernel), kept to measure
  * what fusion saves: launch 1 attends every valid row to the cache only,

@@ -25,7 +25,7 @@ EXPORTS = ("cpattn_create", "cpattn_write_kv", "cpattn_prefill", "cpattn_sync_st
            "cpattn_set_fault_injection", "cpattn_cache_walk", "cpattn_destroy",
            "cpattn_status_string", "cpattn_last_error", "cpattn_prefill_noalloc",
            "cpattn_two_launch_workspace", "cpattn_prefill_two_launch", "cpattn_set_splitkv",
-           "cpattn_splitkv_workspace", "cpattn_cache_walk_from")
+           "cpattn_splitkv_workspace", "cpattn_cache_walk_from", "cpattn_prefill_write_kv")
 
 
 class CpattnError(RuntimeError):
@@ -86,6 +86,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cpattn_splitkv_workspace.restype = I32
     lib.cpattn_cache_walk_from.argtypes = [P, I32, I32, I32P, ctypes.POINTER(U32), I32, I32P]
     lib.cpattn_cache_walk_from.restype = I32
+    lib.cpattn_prefill_write_kv.argtypes = [P, I32, I32P, I32P, P, P, P, P, P, P, P, P]
+    lib.cpattn_prefill_write_kv.restype = I32
     _lib = lib
     return lib
 
@@ -168,6 +170,21 @@ class Context:
         self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
         self._check(self.prefill_raw(cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
                                      out, lse, stream))
+
+    def prefill_write_kv_raw(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
+                             out, lse=None, stream=None) -> int:
+        cl, clp = _i32(cache_lens)
+        ch, chp = _i32(chunk_lens)
+        return self.lib.cpattn_prefill_write_kv(
+            self._h, len(cl), clp, chp, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+            _ptr(v_cache), _ptr(out), _ptr(lse), _stream(stream))
+
+    def prefill_write_kv(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out,
+                         lse=None, stream=None):
+        """Prefill and the chunk's KV-cache write in one launch."""
+        self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
+        self._check(self.prefill_write_kv_raw(cache_lens, chunk_lens, q, k_new, v_new, k_cache,
+                                              v_cache, out, lse, stream))
 
     def two_launch_workspace(self, num_seqs: int) -> int:
         n = ctypes.c_uint64()

@@ -252,7 +252,7 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
                              const int32_t* chunk_lens, const void* q, const void* k_new,
                              const void* v_new, const void* k_cache, const void* v_cache,
                              void* out, float* lse, void* stream, int region, int out_f32,
-                             int split) {
+                             int split, bool write_kv = false) {
   const cpattn_config& c = ctx->cfg;
   const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
   static thread_local cpattn::WorkPlan plan;
@@ -290,6 +290,12 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
   prm.out_f32 = out_f32;
+  if (write_kv) {
+    prm.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    prm.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    prm.k_cache_w = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
+    prm.v_cache_w = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
+  }
   if (ws_need > 0) {
     const size_t o_bytes =
         cpattn::align256(static_cast<size_t>(plan.partial_rows) * NQ * static_cast<size_t>(HD) * 4);
@@ -505,6 +511,25 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   return prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
                         out, lse, stream, cpattn::kRegionAll, 0,
                         ctx->split_ws != nullptr ? ctx->split_policy : cpattn::kSplitOff);
+}
+
+cpattn_status cpattn_prefill_write_kv(cpattn_ctx* ctx, int32_t num_seqs,
+                                      const int32_t* cache_lens, const int32_t* chunk_lens,
+                                      const void* q, const void* k_new, const void* v_new,
+                                      void* k_cache, void* v_cache, void* out, float* lse,
+                                      void* stream) {
+  if (ctx == nullptr) return CPATTN_E_INVALID;
+  cpattn_status s = check_seqs(ctx, num_seqs, cache_lens, chunk_lens);
+  if (s != CPATTN_OK) return s;
+  if (q == nullptr || k_new == nullptr || v_new == nullptr || k_cache == nullptr ||
+      v_cache == nullptr || out == nullptr)
+    return fail(ctx, CPATTN_E_INVALID, "device pointers must not be NULL");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)))
+    return fail(ctx, CPATTN_E_INVALID, "device pointers must be 16-byte aligned");
+  return prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
+                        out, lse, stream, cpattn::kRegionAll, 0,
+                        ctx->split_ws != nullptr ? ctx->split_policy : cpattn::kSplitOff, true);
 }
 
 cpattn_status cpattn_set_splitkv(cpattn_ctx* ctx, void* workspace, uint64_t workspace_bytes,

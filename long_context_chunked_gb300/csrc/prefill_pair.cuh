@@ -314,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_role<HD, SPLIT, true>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
-  } else if (rank == 0) {
+  } else if (warp == kWriterWarp) {
+    if (p.k_cache_w != nullptr) kv_write_lanes<HD>(p, lane);
+  } else if (warp == kMmaWarp && rank == 0) {
     if (lane == 0) mma_role_pair2<HD, SPLIT>(p, sbase, tmem, wait);
   }
   __syncwarp();
