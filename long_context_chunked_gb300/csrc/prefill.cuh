@@ -9,7 +9,7 @@
 // is selected by the value of one scalar (in_cache = v < n_cache): it picks
 // the tensor map and coordinates of the tile loads and the column mask.
 //
-// Roles (320 threads):
+// Roles (352 threads):
 //   warps 0-7  softmax, two warpgroups splitting each row's columns:
 //              tcgen05.ld S (32x32b: one row per thread), value mask, online
 //              (m, l) update with lazy O rescale, P (bf16) back into TMEM
@@ -19,6 +19,7 @@
 //   warp 9     TMEM allocation and the single MMA-issuing thread:
 //              S = Q K^T (both operands in shared memory) and
 //              O += P V (P from TMEM, V from shared memory).
+//   warp 10    the fused KV write (cpattn_prefill_write_kv), else idle.
 //
 // TMEM (512 columns x 128 lanes, fp32): O at [0, HD), S double buffer at
 // [HD, HD+128) and [HD+128, HD+256).  P_t (bf16, two per column) is written
