@@ -82,8 +82,12 @@ typedef struct cpattn_ctx cpattn_ctx; /* opaque */
  * half of every K/V tile), "multicast" (each CTA runs its own MMAs, the pair
  * shares K/V loads), "none" (one CTA per unit).  Results meet the same
  * accuracy in every mode; the bits may differ between modes.
+ * CPATTN_GQA_PACKING ("auto", the default, or "off"), also read here,
+ * controls the packed form of short-chunk launches described at
+ * cpattn_prefill.
  * Errors: E_INVALID (NULL, NQ % NKV != 0, sizes < 1, an unknown
- * CPATTN_PAIRING), E_UNSUPPORTED (HD not 128/256), E_NOMEM.
+ * CPATTN_PAIRING or CPATTN_GQA_PACKING), E_UNSUPPORTED (HD not 128/256),
+ * E_NOMEM.
  */
 cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out);
 
@@ -119,6 +123,11 @@ cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* 
  *   out                 device bf16 [B*C, NQ, HD]; pad rows are not written
  *   lse                 device fp32 [B*C, NQ] natural-log sum-exp of the
  *                       scaled logits, or NULL; pad rows not written
+ * Launches whose chunks are all short (every c_b <= 64) with a power-of-two
+ * group size G = NQ/NKV in [2, 128] run GQA-packed: a work unit's 128
+ * query rows are 128/G tokens x the G q heads of one kv head, instead of
+ * 128 tokens of one q head, so a decode step fills the tensor-core tile
+ * instead of one row of it.
  * One kernel launch -- unless a split-KV workspace is registered
  * (cpattn_set_splitkv) and the batch's plan cuts some walks, in which case a
  * second, merge kernel follows on the same stream.

@@ -36,6 +36,8 @@ struct cpattn_ctx {
   void* split_ws = nullptr;
   size_t split_ws_bytes = 0;
   int split_policy = cpattn::kSplitOff;
+  // GQA packing for short-chunk launches (CPATTN_GQA_PACKING = auto | off).
+  bool gqa_packing = true;
   int debug_flags = 0;
   unsigned long long timeout_ns = 1000ull * 1000 * 1000;
   bool debug_sync = false;
@@ -181,18 +183,40 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
 // The plan's executors and units per work block: SM pairs and q-head pairs
 // when the prefill runs as CTA pairs, else SMs and q heads (148 SMs when no
 // device is present, for host-side planning).
-void plan_shape(const cpattn_ctx* ctx, int* executors, int* units_per_block) {
+void plan_shape(const cpattn_ctx* ctx, bool packed, int* executors, int* units_per_block) {
   const int sms = ctx->num_sms > 0 ? ctx->num_sms : 148;
+  if (packed) {  // one unit per kv head, unpaired
+    *executors = sms;
+    *units_per_block = ctx->cfg.num_kv_heads;
+    return;
+  }
   const bool paired = ctx->pair_mode != 0 && (ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads) % 2 == 0;
   *executors = paired ? sms / 2 : sms;
   *units_per_block = paired ? ctx->cfg.num_q_heads / 2 : ctx->cfg.num_q_heads;
 }
 
-cpattn_status dispatch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st) {
+// GQA packing: a unit's 128 rows become (token, q head of one kv group) when
+// every chunk is short (<= 64 tokens) and the group size G is a power of two
+// in [2, 128], so a decode step fills 128 / G tokens x G heads instead of 1
+// row of 128.  Returns the tokens per row block (128 when not packed).
+constexpr int kPackMaxTokens = 64;
+int pack_block_tokens(const cpattn_ctx* ctx, int32_t num_seqs, const int32_t* chunk_lens,
+                      int region) {
+  const int G = ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads;
+  if (!ctx->gqa_packing || region != cpattn::kRegionAll || G < 2 || G > kBQ || (G & (G - 1)) != 0)
+    return kBQ;
+  for (int b = 0; b < num_seqs; ++b)
+    if (chunk_lens[b] > kPackMaxTokens) return kBQ;
+  return kBQ / G;
+}
+
+cpattn_status dispatch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st,
+                               bool packed) {
   const int HD = ctx->cfg.head_dim;
   const bool split = ctx->cfg.fast_p == 0;
-  // Pair CTAs on adjacent q heads of one kv head when the group size allows.
-  const int mode = (prm->group % 2 == 0) ? ctx->pair_mode : 0;
+  // Pair CTAs on adjacent q heads of one kv head when the group size allows
+  // (packed units hold a whole group already: one CTA each).
+  const int mode = (!packed && prm->group % 2 == 0) ? ctx->pair_mode : 0;
   if (HD == 256) {
     if (mode == 2) return split ? launch_prefill<256, true, 2>(ctx, prm, st)
                                 : launch_prefill<256, false, 2>(ctx, prm, st);
@@ -257,10 +281,12 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
   static thread_local cpattn::WorkPlan plan;
   std::string why;
+  const int block_tokens = pack_block_tokens(ctx, num_seqs, chunk_lens, region);
+  const bool packed = block_tokens != kBQ;
   int executors = 0, units_per_block = 0;
-  plan_shape(ctx, &executors, &units_per_block);
+  plan_shape(ctx, packed, &executors, &units_per_block);
   if (!cpattn::make_plan(c, num_seqs, cache_lens, chunk_lens, region, split, executors,
-                         units_per_block, &plan, &why))
+                         units_per_block, block_tokens, &plan, &why))
     return fail(ctx, CPATTN_E_UNSUPPORTED, why);
   if (plan.blocks.empty()) return CPATTN_OK;
   const size_t ws_need = cpattn::plan_workspace_bytes(plan, NQ, HD);
@@ -285,8 +311,12 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
             encode3d(&prm.tm_k_new_h, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV / 2) &&
             encode3d(&prm.tm_k_cache_h, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV / 2) &&
             encode3d(&prm.tm_v_new_h, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, 64) &&
-            encode3d(&prm.tm_v_cache_h, v_cache, HD, 1, rows, rb, rb, 64, 1, 64);
+            encode3d(&prm.tm_v_cache_h, v_cache, HD, 1, rows, rb, rb, 64, 1, 64) &&
+            (!packed || encode3d(&prm.tm_q_packed, q, HD, NQ, T, rb, rb * NQ, 64,
+                                 static_cast<uint32_t>(NQ / NKV), static_cast<uint32_t>(block_tokens)));
   if (!ok) return fail(ctx, CPATTN_E_CUDA, "cuTensorMapEncodeTiled failed");
+  prm.packed = packed ? 1 : 0;
+  prm.tb = block_tokens;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
   prm.out_f32 = out_f32;
@@ -320,10 +350,10 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
     prm.range[i] = (static_cast<uint32_t>(w.v0) << 16) | static_cast<uint32_t>(w.v1);
     prm.part[i] = w.part;
   }
-  prm.num_units = static_cast<int>(plan.blocks.size()) * NQ;
+  prm.num_units = static_cast<int>(plan.blocks.size()) * (packed ? NKV : NQ);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cpattn_status s = dispatch_prefill(ctx, &prm, st);
+  cpattn_status s = dispatch_prefill(ctx, &prm, st, packed);
   if (s != CPATTN_OK || plan.groups.empty()) return s;
   return launch_splitkv_merge(ctx, plan, prm.ws_o, prm.ws_lse, out, lse, num_seqs, st);
 }
@@ -363,6 +393,14 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   if (!(c.softmax_scale > 0.f)) ctx->cfg.softmax_scale = 1.0f / std::sqrt(static_cast<float>(c.head_dim));
   const char* dbg = std::getenv("CPATTN_DEBUG");
   ctx->debug_sync = dbg != nullptr && dbg[0] == '1';
+  const char* packing = std::getenv("CPATTN_GQA_PACKING");
+  if (packing != nullptr) {
+    if (std::strcmp(packing, "off") == 0) ctx->gqa_packing = false;
+    else if (std::strcmp(packing, "auto") != 0) {
+      delete ctx;
+      return CPATTN_E_INVALID;
+    }
+  }
   const char* pairing = std::getenv("CPATTN_PAIRING");
   if (pairing != nullptr) {
     if (std::strcmp(pairing, "none") == 0) ctx->pair_mode = 0;
@@ -552,10 +590,11 @@ cpattn_status cpattn_splitkv_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
   if (s != CPATTN_OK) return s;
   cpattn::WorkPlan plan;
   std::string why;
+  const int block_tokens = pack_block_tokens(ctx, num_seqs, chunk_lens, cpattn::kRegionAll);
   int executors = 0, units_per_block = 0;
-  plan_shape(ctx, &executors, &units_per_block);
+  plan_shape(ctx, block_tokens != kBQ, &executors, &units_per_block);
   if (!cpattn::make_plan(ctx->cfg, num_seqs, cache_lens, chunk_lens, cpattn::kRegionAll,
-                         max_split_tiles, executors, units_per_block, &plan, &why))
+                         max_split_tiles, executors, units_per_block, block_tokens, &plan, &why))
     return CPATTN_E_UNSUPPORTED;
   *bytes = cpattn::plan_workspace_bytes(plan, ctx->cfg.num_q_heads, ctx->cfg.head_dim);
   if (work_blocks != nullptr) *work_blocks = static_cast<int32_t>(plan.blocks.size());

@@ -90,7 +90,7 @@ inline size_t plan_workspace_bytes(const WorkPlan& w, int nq, int hd) {
 // when the plan exceeds the kernel's tables.
 inline bool make_plan(const cpattn_config& c, int num_seqs, const int32_t* cache_lens,
                       const int32_t* chunk_lens, int region, int split, int executors,
-                      int units_per_block, WorkPlan* plan, std::string* why) {
+                      int units_per_block, int block_tokens, WorkPlan* plan, std::string* why) {
   plan->ncache.assign(num_seqs, 0);
   plan->blocks.clear();
   plan->groups.clear();
@@ -101,15 +101,18 @@ inline bool make_plan(const cpattn_config& c, int num_seqs, const int32_t* cache
     const int nc = cache_tile_count(cache_lens[b], c.num_shards, c.shard_capacity);
     plan->ncache[b] = nc;
     if (region == kRegionCache && nc == 0) continue;  // no cache-only work
-    const int nqb = (chunk_lens[b] + kBQ - 1) / kBQ;
+    // Row blocks of block_tokens chunk tokens (128, or 128 / G when packed);
+    // a block's walk ends with the current tile of its last token.
+    const int nqb = (chunk_lens[b] + block_tokens - 1) / block_tokens;
     for (int qb = 0; qb < nqb; ++qb) {
+      const int last = std::min((qb + 1) * block_tokens, static_cast<int>(chunk_lens[b])) - 1;
       const int v0 = region == kRegionCurrent ? nc : 0;
-      const int v1 = region == kRegionCache ? nc : nc + qb + 1;
+      const int v1 = region == kRegionCache ? nc : nc + last / kBKV + 1;
       if (v1 > kMaxVirtualTiles) {
         *why = "a cache walk longer than 65535 - q blocks tiles";
         return false;
       }
-      rows.push_back({b, qb, v0, v1, std::min(kBQ, chunk_lens[b] - qb * kBQ)});
+      rows.push_back({b, qb, v0, v1, std::min(block_tokens, chunk_lens[b] - qb * block_tokens)});
     }
   }
 
@@ -206,7 +209,7 @@ inline bool make_plan(const cpattn_config& c, int num_seqs, const int32_t* cache
     }
     const int n = r.v1 - r.v0;
     const int part0 = static_cast<int>(plan->partial_rows);
-    plan->groups.push_back({r.b, r.qb * kBQ, r.rows, k, part0});
+    plan->groups.push_back({r.b, r.qb * block_tokens, r.rows, k, part0});
     for (int s = 0; s < k; ++s) {
       const int a = r.v0 + static_cast<int>(static_cast<long long>(n) * s / k);
       const int e = r.v0 + static_cast<int>(static_cast<long long>(n) * (s + 1) / k);

@@ -53,6 +53,7 @@ struct PrefillParams {
   CUtensorMap tm_k_cache_h;  // as tm_k_cache, box 64 x 1 x 64
   CUtensorMap tm_v_new_h;    // as tm_v_new,   box 64 x 1 x 64 (2-SM MMA pairs)
   CUtensorMap tm_v_cache_h;  // as tm_v_cache, box 64 x 1 x 64
+  CUtensorMap tm_q_packed;   // as tm_q,       box 64 x G x 128/G (GQA-packed units)
   __nv_bfloat16* out;
   float* lse;
   int* status;
@@ -61,6 +62,11 @@ struct PrefillParams {
   // out_f32: O is written to `out` as fp32 (the two-launch variant's partial
   // results) instead of bf16.
   int out_f32;
+  // GQA packing (launches whose chunks are all short): a unit is (sequence,
+  // kv head, block of tb = 128 / group tokens) and its 128 rows are (token
+  // t0 + r / group, q head g * group + r % group).  0: a unit is (sequence, q
+  // head, block of 128 tokens).
+  int packed, tb;
   float scale_log2;
   // Fused KV write (null: none): the chunk's K/V rows, read from k_new /
   // v_new, are also copied into the striped caches k_cache_w / v_cache_w.
@@ -140,6 +146,8 @@ struct Layout {
 static_assert(sizeof(PrefillParams) <= 32764, "kernel parameter budget");
 
 struct Unit {
+  // h: the q head (packed: the group's first q head); qb: the row block (packed:
+  // the token block); q0: its first token.
   int b, h, g, qb, q0, L, c, n_cache;
   int v0, n_tiles;  // this work block's tiles: virtual indices [v0, v0 + n_tiles)
   int part;         // -1, or the first partial row of a split-KV piece
@@ -147,13 +155,15 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
   Unit U;
-  const int blk = u / p.nq;
-  U.h = u - blk * p.nq;
+  const int per = p.packed ? p.nkv : p.nq;  // units per work block
+  const int blk = u / per;
+  const int k = u - blk * per;
   const uint32_t e = p.blocks[blk];
   U.b = static_cast<int>(e >> 16);
   U.qb = static_cast<int>(e & 0xFFFFu);
-  U.g = U.h / p.group;
-  U.q0 = U.qb * kBQ;
+  U.g = p.packed ? k : k / p.group;
+  U.h = p.packed ? k * p.group : k;
+  U.q0 = U.qb * (p.packed ? p.tb : kBQ);
   U.L = p.seqs[U.b].cache_len;
   U.c = p.seqs[U.b].chunk_len;
   U.n_cache = p.seqs[U.b].n_cache_tiles;
@@ -240,8 +250,8 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
     }
     mbar_arrive_expect_tx(bar(Ly::B_QFULL), Ly::Q_BYTES);
     for (int c = 0; c < Ly::KCH; ++c)
-      tma_load_3d(sbase + Ly::OFF_Q + c * (kBQ * 128), &p.tm_q, bar(Ly::B_QFULL), 64 * c, U.h,
-                  U.b * p.C + U.q0);
+      tma_load_3d(sbase + Ly::OFF_Q + c * (kBQ * 128), p.packed ? &p.tm_q_packed : &p.tm_q,
+                  bar(Ly::B_QFULL), 64 * c, U.h, U.b * p.C + U.q0);
     ++q_issued;
 
     const int head_row = ((U.b * p.nkv + U.g) * p.P) * p.S;
@@ -308,7 +318,7 @@ __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane)
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     const Unit U = decode_unit(p, u);
     if (U.h % p.group != 0 || U.v0 != 0) continue;
-    const int rows = min(kBQ, U.c - U.q0);
+    const int rows = min(p.packed ? p.tb : kBQ, U.c - U.q0);  // valid tokens of the block
     const long long head_row = static_cast<long long>(U.b * p.nkv + U.g) * p.P * p.S;
     for (int i = lane; i < rows * VECS; i += 32) {
       const int r = i / VECS, x = i - r * VECS;
@@ -473,6 +483,9 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
     const Unit U = decode_unit(p, u);
+    // This row's token (within the chunk) and q head.
+    const int tok = U.q0 + (p.packed ? r / p.group : r);
+    const int head = p.packed ? U.h + r % p.group : U.h;
     CacheWalk walk;
     walk.init(U.L, p.P, p.S);
     walk.skip(U.v0 < U.n_cache ? U.v0 : U.n_cache);
@@ -501,7 +514,10 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
           walk.column_mask(tile, mw);
         }
       } else {
-        const int lim = (va - U.n_cache == U.qb) ? r + 1 : kBKV;
+        // Causal: current tile j holds chunk tokens 128 j .. 128 j + 127; this
+        // row sees those <= tok.
+        const int lim0 = tok - kBKV * (va - U.n_cache) + 1;
+        const int lim = lim0 < 0 ? 0 : (lim0 > kBKV ? kBKV : lim0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) mw[q] = causal_word(lim, q);
       }
@@ -669,14 +685,15 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       continue;
     }
     tc_fence_after();
-    const int row = U.q0 + r;
+    const int row = tok;
     const bool valid = row < U.c;
     const float inv_l = 1.f / l_row;
     // A split-KV piece writes fp32 O / l and its LSE to its partial rows; a
     // whole unit writes the output row (bf16, or fp32 when out_f32).
     const bool partial = U.part >= 0;
-    const long long tok = static_cast<long long>(U.b) * p.C + row;
-    const long long orow_i = (partial ? static_cast<long long>(U.part + r) : tok) * p.nq + U.h;
+    const long long tok_g = static_cast<long long>(U.b) * p.C + row;  // token-order row
+    const long long orow_i =
+        (partial ? static_cast<long long>(U.part + (row - U.q0)) : tok_g) * p.nq + head;
     const bool f32 = partial || p.out_f32 != 0;
     float* lse_out = partial ? p.ws_lse : p.lse;
     uint4* orow = reinterpret_cast<uint4*>(p.out + orow_i * HD + h * OCOLS);

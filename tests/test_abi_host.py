@@ -79,6 +79,22 @@ def test_pairing_mode_from_environment(lib, monkeypatch, value, ok):
         assert e.value.status == cp.E_INVALID
 
 
+@pytest.mark.parametrize("value,ok", [("auto", True), ("off", True), ("on", False)])
+def test_gqa_packing_from_environment(lib, monkeypatch, value, ok):
+    monkeypatch.setenv("CPATTN_GQA_PACKING", value)
+    if ok:
+        ctx = cp.Context(32, 2, 256, 8, 1000, 64)
+        # A decode step is packed (one 8-token block) unless packing is off.
+        _, blocks = ctx.splitkv_workspace([5000], [1], 1 << 20)
+        assert blocks == 1
+        _, blocks = ctx.splitkv_workspace([5000, 5000], [64, 1], 1 << 20)
+        assert blocks == (8 + 1 if value == "auto" else 2)
+    else:
+        with pytest.raises(cp.CpattnError) as e:
+            cp.Context(32, 2, 256, 8, 1000, 64)
+        assert e.value.status == cp.E_INVALID
+
+
 def test_prefill_and_write_validation(lib):
     ctx = cp.Context(8, 2, 128, 2, 64, 32)
     A = 256  # a 16-byte-aligned stand-in pointer; nothing is launched
