@@ -257,15 +257,15 @@ cpattn_status launch_splitkv_merge(cpattn_ctx* ctx, const cpattn::WorkPlan& plan
     mp.g_n[g] = G.n;
     mp.g_part0[g] = G.part0;
     mp.g_prefix[g] = total;
-    total += static_cast<long long>(G.rows) * c.num_q_heads * (c.head_dim / 8);
+    total += static_cast<long long>(G.rows) * c.num_q_heads;  // (row, head) pairs
   }
   mp.g_prefix[mp.num_groups] = total;
   mp.total = total;
   (void)num_seqs;
-  const long long want = (total + 255) / 256;
+  // One CTA per (row, head), grid-stride beyond a few waves.
   const int grid = static_cast<int>(std::max<long long>(
-      1, std::min<long long>(want, static_cast<long long>(std::max(ctx->num_sms, 1)) * 8)));
-  cpattn::splitkv_merge_kernel<<<grid, 256, 0, st>>>(mp);
+      1, std::min<long long>(total, static_cast<long long>(std::max(ctx->num_sms, 1)) * 16)));
+  cpattn::splitkv_merge_kernel<<<grid, 32 * cpattn::kMergeWarps, 0, st>>>(mp);
   return after_launch(ctx, st, "split-KV merge launch");
 }
 

@@ -77,8 +77,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const __grid_constant__ 
 // fp32 and LSE_s) over disjoint key sets; the softmax over their union is
 //   m = max_s LSE_s,  w_s = exp(LSE_s - m),
 //   O = sum_s w_s O_s / sum_s w_s,  LSE = m + log(sum_s w_s).
-// Piece s of a group has its partial rows at part0 + s * rows.  HBM-bound:
-// one thread per 8 consecutive output elements of one (row, head).
+// Piece s of a group has its partial rows at part0 + s * rows.
 constexpr int kMaxSplitGroups = 256;
 
 struct SplitMergeParams {
@@ -87,56 +86,84 @@ struct SplitMergeParams {
   __nv_bfloat16* out;   // [T, NQ, HD]
   float* lse;           // [T, NQ] or null
   int num_groups, C, nq, hd;
-  long long total;      // sum over groups of rows * NQ * HD / 8
+  long long total;      // (row, head) pairs: sum over groups of rows * NQ
   int g_b[kMaxSplitGroups], g_q0[kMaxSplitGroups], g_rows[kMaxSplitGroups];
   int g_n[kMaxSplitGroups], g_part0[kMaxSplitGroups];
   long long g_prefix[kMaxSplitGroups + 1];
 };
 
-__global__ void __launch_bounds__(256) splitkv_merge_kernel(const __grid_constant__ SplitMergeParams p) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  const int per_head = p.hd / 8;
-  const int per_row = p.nq * per_head;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-       idx < p.total; idx += stride) {
+// One CTA of kMergeWarps warps per (row, head) of a group.  Every warp reads
+// all n piece LSEs (a few per lane) and reduces their max and weight sum
+// itself; warp w then accumulates the pieces s = w, w + kMergeWarps, ... for
+// output elements 8j .. 8j + 7 in lane j, and the warps' partial sums are
+// added through shared memory.  A decode step has few (row, head) pairs and
+// many pieces: spreading the pieces over warps turns n dependent memory
+// round trips into n / kMergeWarps.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeMaxHd = 256;
+
+__global__ void __launch_bounds__(32 * kMergeWarps) splitkv_merge_kernel(
+    const __grid_constant__ SplitMergeParams p) {
+  __shared__ float part[kMergeWarps][kMergeMaxHd];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (long long it = blockIdx.x; it < p.total; it += gridDim.x) {
     int lo = 0, hi = p.num_groups - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.g_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+      if (p.g_prefix[mid] <= it) lo = mid; else hi = mid - 1;
     }
     const int g = lo;
-    const long long local = idx - p.g_prefix[g];
-    const int r = static_cast<int>(local / per_row);         // row within the block
-    const int rem = static_cast<int>(local - static_cast<long long>(r) * per_row);
-    const int h = rem / per_head;
-    const int part8 = rem - h * per_head;
+    const int local = static_cast<int>(it - p.g_prefix[g]);
+    const int r = local / p.nq, h = local - r * p.nq;
     const int n = p.g_n[g];
+    const long long pr0 = static_cast<long long>(p.g_part0[g]) + r;  // piece s: pr0 + s * rows
+    const long long pstride = p.g_rows[g];
     float m = -INFINITY;
-    for (int s = 0; s < n; ++s) {
-      const long long pr = static_cast<long long>(p.g_part0[g]) + static_cast<long long>(s) * p.g_rows[g] + r;
-      m = fmaxf(m, p.ws_lse[pr * p.nq + h]);
-    }
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = lane; s < n; s += 32) m = fmaxf(m, p.ws_lse[(pr0 + s * pstride) * p.nq + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     float wsum = 0.f;
-    for (int s = 0; s < n; ++s) {
-      const long long pr = static_cast<long long>(p.g_part0[g]) + static_cast<long long>(s) * p.g_rows[g] + r;
-      const float w = __expf(p.ws_lse[pr * p.nq + h] - m);
-      wsum += w;
-      const float* src = p.ws_o + (pr * p.nq + h) * p.hd + part8 * 8;
-      const float4 a = *reinterpret_cast<const float4*>(src);
-      const float4 b = *reinterpret_cast<const float4*>(src + 4);
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-      acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    for (int s = lane; s < n; s += 32) wsum += __expf(p.ws_lse[(pr0 + s * pstride) * p.nq + h] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
+    const int e = lane * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (e < p.hd) {
+#pragma unroll 2
+      for (int s = warp; s < n; s += kMergeWarps) {
+        const long long pr = pr0 + s * pstride;
+        const float w = __expf(p.ws_lse[pr * p.nq + h] - m);
+        const float* src = p.ws_o + (pr * p.nq + h) * p.hd + e;
+        const float4 a = *reinterpret_cast<const float4*>(src);
+        const float4 b = *reinterpret_cast<const float4*>(src + 4);
+        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) part[warp][e + i] = acc[i];
     }
-    const float inv = 1.f / wsum;
-    const long long tok = static_cast<long long>(p.g_b[g]) * p.C + p.g_q0[g] + r;
-    uint4 o;
-    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(p.out + (tok * p.nq + h) * p.hd + part8 * 8) = o;
-    if (part8 == 0 && p.lse != nullptr) p.lse[tok * p.nq + h] = m + __logf(wsum);
+    __syncthreads();
+    // Thread t sums element t over the warps' partials.
+    for (int x = threadIdx.x; x < p.hd; x += blockDim.x) {
+      float v = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kMergeWarps; ++w2) v += part[w2][x];
+      part[0][x] = v;  // each element read-then-written by one thread only
+    }
+    __syncthreads();
+    if (warp == 0 && e < p.hd) {
+      const float inv = 1.f / wsum;
+      const long long tok = static_cast<long long>(p.g_b[g]) * p.C + p.g_q0[g] + r;
+      const float* v = &part[0][e];
+      uint4 o;
+      o.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+      o.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+      o.z = pack_bf16x2(v[4] * inv, v[5] * inv);
+      o.w = pack_bf16x2(v[6] * inv, v[7] * inv);
+      *reinterpret_cast<uint4*>(p.out + (tok * p.nq + h) * p.hd + e) = o;
+      if (lane == 0 && p.lse != nullptr) p.lse[tok * p.nq + h] = m + __logf(wsum);
+    }
+    __syncthreads();  // part[] is reused by the next (row, head)
   }
 }
 
