@@ -265,7 +265,17 @@ cpattn_status launch_splitkv_merge(cpattn_ctx* ctx, const cpattn::WorkPlan& plan
   // One CTA per (row, head), grid-stride beyond a few waves.
   const int grid = static_cast<int>(std::max<long long>(
       1, std::min<long long>(total, static_cast<long long>(std::max(ctx->num_sms, 1)) * 16)));
-  cpattn::splitkv_merge_kernel<<<grid, 32 * cpattn::kMergeWarps, 0, st>>>(mp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(32 * cpattn::kMergeWarps, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, cpattn::splitkv_merge_kernel, mp);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "split-KV merge launch");
   return after_launch(ctx, st, "split-KV merge launch");
 }
 

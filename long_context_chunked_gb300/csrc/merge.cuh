@@ -106,6 +106,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) splitkv_merge_kernel(
     const __grid_constant__ SplitMergeParams p) {
   __shared__ float part[kMergeWarps][kMergeMaxHd];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Launched as a programmatic dependent of the prefill kernel: the launch
+  // overlaps the prefill's tail; this waits until that grid has completed
+  // and its partial rows are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (long long it = blockIdx.x; it < p.total; it += gridDim.x) {
     int lo = 0, hi = p.num_groups - 1;
     while (lo < hi) {
