@@ -44,10 +44,11 @@ def load_peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
-# Device sources each profiled kernel is built from (its launch code too).
+# Device sources each profiled kernel is built from, and the work plan that
+# shapes its launch; a DRAM record holds while these are unchanged.
 KERNEL_SOURCES = {
-    "prefill": ("cpattn.cu", "prefill.cuh", "prefill_pair.cuh", "walk.cuh", "ptx.cuh"),
-    "write_kv": ("cpattn.cu", "write_kv.cuh"),
+    "prefill": ("prefill.cuh", "prefill_pair.cuh", "walk.cuh", "ptx.cuh", "plan.h"),
+    "write_kv": ("write_kv.cuh",),
 }
 
 
