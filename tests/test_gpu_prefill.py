@@ -143,3 +143,42 @@ def test_repeatable_and_write_order_independent():
     ctx.write_kv(w.cache_lens, w.chunk_lens, dc.k_new.t, dc.v_new.t, dc.k_cache.t, dc.v_cache.t)
     dc.prefill(ctx)
     assert np.array_equal(first, dc.out.bits())
+
+
+@pytest.mark.parametrize("hd,nq,nkv", [(128, 4, 2), (256, 8, 2), (128, 3, 3)])
+def test_rescale_on_every_tile(hd, nq, nkv):
+    """Keys constant along each row, stepping up by 0.5 per tile in walk
+    order (cache flat rows, then the chunk's tiles), queries all ones: every
+    tile's row max exceeds the running max by sqrt(HD) * 0.5 * log2(e) > 8, so
+    the lazy rescale of O -- and its wait for the previous tile's P.V --
+    runs on every tile of every unit, in the paired and unpaired kernels."""
+    w = small(f"resc{hd}", (1500, 300), (300, 200), 320, nq=nq, nkv=nkv, hd=hd, shards=3,
+              shard_capacity=700, seed=41 + hd)
+    case = make_case(w)
+    one = np.uint16(0x3F80)
+    case.q_bits[...] = one
+
+    def bf16_of(x):  # exact: multiples of 0.5 below 256
+        return oracle.bf16_bits(torch.tensor([float(x)]).to(torch.bfloat16))[0]
+
+    kc = case.k_cache_bits  # [B, NKV, P, S, HD]
+    B, NKV, P, S, HD = kc.shape
+    top = 0
+    for b in range(B):
+        for s in range(P):
+            for r in range(S):
+                f = s * S + r  # flat row of the (sequence, kv head) walk
+                kc[b, :, s, r, :] = bf16_of(0.5 * (f // 128))
+        top = max(top, (P * S) // 128 + 1)
+    for b, c in enumerate(w.chunk_lens):
+        for i in range(c):
+            case.k_new_bits[b * w.chunk + i, :, :] = bf16_of(0.5 * (top + i // 128))
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w)
+    dc.prefill(ctx)
+    ref, ref_lse = case.oracle_full()
+    v = dc.valid_rows()
+    compare(to_f64(dc.out.bits())[v], ref[v], f"rescale every tile, HD={hd}")
+    lse = dc.lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse[v] - ref_lse[v])) / max(1.0, np.max(np.abs(ref_lse[v]))) < 2e-3
+    assert dc.guards_intact()
