@@ -126,3 +126,18 @@ def test_workspace_off_again():
     ref, _ = case.oracle_full()
     v = dc.valid_rows()
     compare(to_f64(dc.out.bits())[v], ref[v], "after turning split-KV off")
+
+
+FULL_DECODE = [
+    small("dec_1x128k", (126976,), (1,), 1, nq=32, nkv=2, hd=256, shards=8, seed=91),
+    small("dec_8x32k", (32768,) * 8, (1,) * 8, 1, nq=32, nkv=2, hd=256, shards=8, seed=92),
+]
+
+
+@pytest.mark.parametrize("w", FULL_DECODE, ids=[w.name for w in FULL_DECODE])
+def test_full_size_decode_every_row(w):
+    """The decode workloads `bench.py --splitkv` times, at full size in the
+    launch configuration it times (GQA-packed, automatic split-KV plan): a
+    decode step has only NQ output rows per sequence, so every one of them
+    is compared with the oracle."""
+    _run(w, 0)
