@@ -334,6 +334,9 @@ __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane)
 }
 
 // ------------------------------------------------------------- MMA issuer
+// Run by the whole MMA warp: control flow and operands are warp-uniform (every
+// wait's outcome is agreed by the warp), and each MMA and commit is issued by
+// one elected lane.
 template <int HD, bool SPLIT, bool MC>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                          const BoundedWait& wait) {
@@ -344,6 +347,9 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   RingPos rp;
   uint32_t tile_ctr = 0, units = 0;
   bool ok = true;
+  auto wwait = [&](uint32_t b, uint32_t parity, int site) {
+    return __all_sync(0xFFFFFFFFu, wait(b, parity, site));
+  };
   // A slot is released to the producers of every CTA that shares it.
   auto release_slot = [](uint32_t b) {
     if (MC) mma_commit_mc(b, 0x3); else mma_commit(b);
@@ -366,11 +372,11 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   // O (+)= P_w V_w, P_w from the S buffer of global tile t.
   auto issue_pv = [&](int w, uint32_t t) {
     const uint32_t sb = t & 1u;
-    if (!wait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
+    if (!wwait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
     tc_fence_after();
     const uint32_t p_tmem = tmem + HD + sb * kBKV;
     for (int j = 0; j < Ly::VSUB; ++j) {
-      if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
+      if (!wwait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
       tc_fence_after();
       const uint32_t vb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
 #pragma unroll
@@ -394,7 +400,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
 
   for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
     const Unit U = decode_unit(p, u);
-    if (!wait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
+    if (!wwait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
       ok = false;
       break;
     }
@@ -403,7 +409,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
       const uint32_t sb = tile_ctr & 1u;
       const uint32_t s_tmem = tmem + HD + sb * kBKV;
       for (int c = 0; c < Ly::KCH; ++c) {
-        if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) {
+        if (!wwait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) {
           ok = false;
           break;
         }
@@ -783,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   } else if (warp == kWriterWarp) {
     if (p.k_cache_w != nullptr) kv_write_lanes<HD>(p, lane);
   } else {
-    if (lane == 0) mma_role<HD, SPLIT, MC>(p, sbase, tmem, wait);
+    mma_role<HD, SPLIT, MC>(p, sbase, tmem, wait);
   }
   __syncwarp();
   tc_fence_before();

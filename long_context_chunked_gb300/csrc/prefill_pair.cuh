@@ -156,7 +156,9 @@ __device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint
 }
 
 // ------------------------------------------------------------- MMA issuer
-// Leader CTA only, one thread.
+// Leader CTA only, the whole MMA warp: control flow and operands are
+// warp-uniform (every wait's outcome is agreed by the warp), and each MMA and
+// commit is issued by one elected lane.
 template <int HD, bool SPLIT>
 __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t sbase,
                                                uint32_t tmem, const BoundedWait& wait) {
@@ -168,6 +170,9 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
   RingPos rp;
   uint32_t tile_ctr = 0, units = 0;
   bool ok = true;
+  auto wwait = [&](uint32_t b, uint32_t parity, int site) {
+    return __all_sync(0xFFFFFFFFu, wait(b, parity, site));
+  };
 #ifdef CPATTN_SERIALIZE_MMA
   // Race-detection build: every MMA group completes before the MMA thread
   // moves on (see prefill.cuh).
@@ -185,11 +190,11 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
   // O (+)= P_w V_w over both CTAs' rows, P_w from the S buffer of tile t.
   auto issue_pv = [&](int w, uint32_t t) {
     const uint32_t sb = t & 1u;
-    if (!wait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
+    if (!wwait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
     tc_fence_after();
     const uint32_t p_tmem = tmem + HD + sb * kBKV;
     for (int j = 0; j < Pl::VSLOTS; ++j) {
-      if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
+      if (!wwait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
       tc_fence_after();
       const uint32_t vb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
 #pragma unroll
@@ -212,7 +217,7 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
 
   for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
     const Unit U = decode_unit(p, u);
-    if (!wait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
+    if (!wwait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
       ok = false;
       break;
     }
@@ -221,7 +226,7 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
       const uint32_t sb = tile_ctr & 1u;
       const uint32_t s_tmem = tmem + HD + sb * kBKV;
       for (int j = 0; j < Pl::KSLOTS; ++j) {
-        if (!wait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) {
+        if (!wwait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) {
           ok = false;
           break;
         }
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWriterWarp) {
     if (p.k_cache_w != nullptr) kv_write_lanes<HD>(p, lane);
   } else if (warp == kMmaWarp && rank == 0) {
-    if (lane == 0) mma_role_pair2<HD, SPLIT>(p, sbase, tmem, wait);
+    mma_role_pair2<HD, SPLIT>(p, sbase, tmem, wait);
   }
   __syncwarp();
   tc_fence_before();
