@@ -149,20 +149,22 @@ class DeviceState:
     order, and the striped caches filled with the logical prefix by the
     library's own KV write."""
 
-    def __init__(self, w: Workload, device, fast_p: bool = False, variant: str = "fused"):
+    def __init__(self, w: Workload, device, fast_p: bool = False, variant: str = "fused",
+                 v_f16: bool = False):
         import torch
         import long_context_chunked_gb300 as cp
         self.w = w
         self.variant = variant
         inp = generate(w)
         self.inp = inp
-        self.ctx = cp.Context.for_workload(w, fast_p=fast_p)
+        self.ctx = cp.Context.for_workload(w, fast_p=fast_p, v_cache_f16=v_f16)
         self.q = inp.q.to(device)
         self.k_new = inp.k_new.to(device)
         self.v_new = inp.v_new.to(device)
         shape = (w.num_seqs, w.num_kv_heads, w.shards, w.shard_capacity, w.head_dim)
         self.k_cache = torch.zeros(shape, dtype=torch.bfloat16, device=device)
-        self.v_cache = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        self.v_cache = torch.zeros(shape, dtype=torch.float16 if v_f16 else torch.bfloat16,
+                                   device=device)
         self.out = torch.zeros_like(self.q)
         self.workspace = None
         if variant == "two_launch":
@@ -171,7 +173,7 @@ class DeviceState:
         lmax = max(w.cache_lens)
         if lmax:
             fill = cp.Context(w.num_q_heads, w.num_kv_heads, w.head_dim, w.shards,
-                              w.shard_capacity, lmax, w.scale)
+                              w.shard_capacity, lmax, w.scale, v_cache_f16=v_f16)
             kl = torch.zeros((w.num_seqs * lmax, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16)
             vl = torch.zeros_like(kl)
             for b, L in enumerate(w.cache_lens):
@@ -542,6 +544,17 @@ def run_splitkv(fast_p=False, reps=20, seed=11):
         del q, kn, vn, kc, vc, out, ws, ctx
 
 
+def precision_label(fast_p: bool, v_f16: bool) -> str:
+    cur = "P rounded to bf16" if fast_p else "bf16 hi+lo P pair"
+    if v_f16:
+        return f"cache tiles: fp16 P x fp16 V; current tiles: {cur}"
+    return "fast_p (P rounded to bf16)" if fast_p else "accurate P (bf16 hi+lo pair)"
+
+
+def traffic_key(kname: str, workload: str, fast_p: bool, v_f16: bool) -> str:
+    return f"{kname}:{workload}:{'fast_p' if fast_p else 'accurate'}" + (":vf16" if v_f16 else "")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -550,6 +563,9 @@ def main():
     ap.add_argument("--impl", default="cpattn", choices=["cpattn", "reference"])
     ap.add_argument("--config", default="32k", choices=sorted(BY_NAME))
     ap.add_argument("--fast-p", action="store_true", help="P rounded once to bf16")
+    ap.add_argument("--v-cache", default="bf16", choices=["bf16", "f16"],
+                    help="V cache format: f16 makes cache tiles take P in fp16 (one P.V "
+                         "product at the accurate mode's precision)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", default="fused", choices=["fused", "two_launch", "fused_write"],
                     help="fused_write: the KV write inside the prefill launch; "
@@ -585,7 +601,8 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
     w = BY_NAME[args.config]
-    st = DeviceState(w, device, fast_p=args.fast_p, variant=args.variant)
+    v_f16 = args.v_cache == "f16"
+    st = DeviceState(w, device, fast_p=args.fast_p, variant=args.variant, v_f16=v_f16)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
     if world > 1:
@@ -611,11 +628,12 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16+f16" if v_f16 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16, 1% of keys doubled)",
         "config": {"workload": w.name, "description": w.description,
-                   "precision": "fast_p (P rounded to bf16)" if args.fast_p else
-                   "accurate P (bf16 hi+lo pair)",
+                   "precision": precision_label(args.fast_p, v_f16),
+                   "v_cache": args.v_cache,
                    "l2": "flushed between steps (512 MiB write)",
                    "parallelism": f"replicas x{world}", "variant": args.variant},
         "prefill_ms": round(pf, 4), "write_kv_ms": round(kv_ms, 4),
@@ -626,7 +644,7 @@ def main():
                      "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
                      "kernel": kname,
                      "traffic": profiled_traffic(
-                         "prefill", f"{kname}:{w.name}:{'fast_p' if args.fast_p else 'accurate'}")},
+                         "prefill", traffic_key(kname, w.name, args.fast_p, v_f16))},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

@@ -46,7 +46,8 @@ typedef enum {
   CPATTN_E_UNSUPPORTED = 2,  /* valid but outside what this build handles */
   CPATTN_E_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
   CPATTN_E_NOMEM = 4,        /* host or device allocation failed (create only) */
-  CPATTN_E_TIMEOUT = 5       /* a device-side bounded wait expired; context still usable */
+  CPATTN_E_TIMEOUT = 5,      /* a device-side bounded wait expired; context still usable */
+  CPATTN_E_RANGE = 6         /* a value written to an fp16 V cache lies outside fp16's range */
 } cpattn_status;
 
 typedef struct {
@@ -62,6 +63,18 @@ typedef struct {
                               significant bits); 1: P rounded once to bf16 (one
                               product, 1.5x fewer MMA FLOPs, relative RMS error
                               about 2.2e-3 instead of 1.7e-3 on N(0,1) inputs) */
+  int32_t v_cache_f16;     /* 0 (default): the V cache holds bf16, as k_cache;
+                              1: the V cache holds fp16.  cpattn_write_kv then
+                              converts each bf16 value of v_new to fp16
+                              (round to nearest even: exact for normal values
+                              within fp16's range, |v| <= 65504); a value it
+                              cannot represent finitely is reported by the next
+                              cpattn_sync_status as CPATTN_E_RANGE.  Prefill
+                              then takes P in fp16 for cache tiles: one P.V
+                              product (11-bit P, relative RMS error about 1.7e-3
+                              on N(0,1) inputs, as the bf16 hi + lo pair) at the
+                              cost of fast_p.  Current-chunk tiles still read
+                              bf16 v_new and follow fast_p. */
 } cpattn_config;
 
 typedef struct cpattn_ctx cpattn_ctx; /* opaque */
@@ -96,12 +109,16 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out);
  * bit-exact).  For every sequence b, valid chunk row i < c_b (token position
  * t = L_b + i) and kv head g:
  *   k_cache[b, g, t mod P, t div P, :] = k_new[b*C + i, g, :]   (same for V)
- * A pure bit copy.  Pad rows are not written; no other cache row is touched.
+ * A pure bit copy, except that an fp16 V cache (cpattn_config.v_cache_f16)
+ * receives each V value converted to fp16 (round to nearest even); a value
+ * beyond fp16's finite range makes the next cpattn_sync_status return
+ * CPATTN_E_RANGE.  Pad rows are not written; no other cache row is touched.
  *   num_seqs            B, 1..CPATTN_MAX_SEQS
  *   cache_lens[B]       host int32, L_b >= 0
  *   chunk_lens[B]       host int32, 0 <= c_b <= C, and L_b + c_b <= P*S
  *   k_new, v_new        device bf16 [B*C, NKV, HD], token order
- *   k_cache, v_cache    device bf16 [B, NKV, P, S, HD], written in place
+ *   k_cache             device bf16 [B, NKV, P, S, HD], written in place
+ *   v_cache             the same, bf16 or (v_cache_f16) fp16
  * Errors: E_INVALID, E_CUDA.
  */
 cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* cache_lens,

@@ -16,7 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 # CPATTN_LIBRARY overrides the library path (e.g. an instrumented build).
 LIB_PATH = os.environ.get("CPATTN_LIBRARY") or os.path.join(_PKG, "libcpattn.so")
 
-OK, E_INVALID, E_UNSUPPORTED, E_CUDA, E_NOMEM, E_TIMEOUT = range(6)
+OK, E_INVALID, E_UNSUPPORTED, E_CUDA, E_NOMEM, E_TIMEOUT, E_RANGE = range(7)
 MAX_SEQS = 128
 MAX_ROW_BLOCKS = 2048
 
@@ -38,7 +38,8 @@ class Config(ctypes.Structure):
     _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("num_shards", ctypes.c_int32),
                 ("shard_capacity", ctypes.c_int32), ("chunk_size", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float), ("fast_p", ctypes.c_int32)]
+                ("softmax_scale", ctypes.c_float), ("fast_p", ctypes.c_int32),
+                ("v_cache_f16", ctypes.c_int32)]
 
 
 _lib = None
@@ -120,10 +121,11 @@ class Context:
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, num_shards: int,
                  shard_capacity: int, chunk_size: int, softmax_scale: float = 0.0,
-                 fast_p: bool = False):
+                 fast_p: bool = False, v_cache_f16: bool = False):
         self.lib = load()
         self.cfg = Config(num_q_heads, num_kv_heads, head_dim, num_shards, shard_capacity,
-                          chunk_size, softmax_scale, int(bool(fast_p)))
+                          chunk_size, softmax_scale, int(bool(fast_p)), int(bool(v_cache_f16)))
+        self.v_cache_f16 = bool(v_cache_f16)
         h = ctypes.c_void_p()
         st = self.lib.cpattn_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if st != OK:
@@ -131,9 +133,9 @@ class Context:
         self._h = h
 
     @classmethod
-    def for_workload(cls, w, fast_p: bool = False) -> "Context":
+    def for_workload(cls, w, fast_p: bool = False, v_cache_f16: bool = False) -> "Context":
         return cls(w.num_q_heads, w.num_kv_heads, w.head_dim, w.shards, w.shard_capacity,
-                   w.chunk, w.scale, fast_p)
+                   w.chunk, w.scale, fast_p, v_cache_f16)
 
     # -- status --------------------------------------------------------
     def _check(self, st: int):
@@ -153,7 +155,7 @@ class Context:
                                         _ptr(k_cache), _ptr(v_cache), _stream(stream))
 
     def write_kv(self, cache_lens, chunk_lens, k_new, v_new, k_cache, v_cache, stream=None):
-        self._check_tensors((k_new, v_new, k_cache, v_cache))
+        self._check_tensors((k_new, v_new, k_cache), v_cache)
         self._check(self.write_kv_raw(cache_lens, chunk_lens, k_new, v_new, k_cache, v_cache,
                                       stream))
 
@@ -167,7 +169,7 @@ class Context:
 
     def prefill(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out, lse=None,
                 stream=None):
-        self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
+        self._check_tensors((q, k_new, v_new, k_cache, out), v_cache)
         self._check(self.prefill_raw(cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
                                      out, lse, stream))
 
@@ -182,7 +184,7 @@ class Context:
     def prefill_write_kv(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out,
                          lse=None, stream=None):
         """Prefill and the chunk's KV-cache write in one launch."""
-        self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
+        self._check_tensors((q, k_new, v_new, k_cache, out), v_cache)
         self._check(self.prefill_write_kv_raw(cache_lens, chunk_lens, q, k_new, v_new, k_cache,
                                               v_cache, out, lse, stream))
 
@@ -194,7 +196,7 @@ class Context:
     def prefill_two_launch(self, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out,
                            workspace, lse=None, stream=None):
         """The removed two-launch variant (cache-only + current-only + LSE merge)."""
-        self._check_tensors((q, k_new, v_new, k_cache, v_cache, out))
+        self._check_tensors((q, k_new, v_new, k_cache, out), v_cache)
         cl, clp = _i32(cache_lens)
         ch, chp = _i32(chunk_lens)
         nbytes = workspace.numel() * workspace.element_size()
@@ -254,14 +256,16 @@ class Context:
         except Exception:
             pass
 
-    @staticmethod
-    def _check_tensors(ts):
+    def _check_tensors(self, ts, v_cache):
+        """bf16 tensors, and the V cache in the context's format (fp16 with
+        v_cache_f16, else bf16); contiguous, on the GPU."""
         import torch
-        for t in ts:
+        want_v = torch.float16 if self.v_cache_f16 else torch.bfloat16
+        for t, want in [(t, torch.bfloat16) for t in ts] + [(v_cache, want_v)]:
             if t is None or isinstance(t, int):
                 continue
-            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-                raise ValueError("expected contiguous bf16 CUDA tensors")
+            if t.dtype != want or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"expected a contiguous {want} CUDA tensor, got {t.dtype}")
 
 
 def prefill_noalloc(cfg: Config, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache, out,

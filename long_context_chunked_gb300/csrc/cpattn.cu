@@ -27,7 +27,7 @@ struct cpattn_ctx {
   int device = -1;
   int num_sms = 0;
   int* d_status = nullptr;           // device status word (timeouts)
-  int grid_cap[2][2][3] = {};  // [HD == 256][split P][pairing mode]: 0 until set up
+  int grid_cap[2][2][3][2] = {};  // [HD == 256][split P][pairing mode][fp16 V cache]: 0 until set up
   // CTA pairing for even group sizes (CPATTN_PAIRING = mma2 | multicast | none):
   // 2 = 2-SM MMA pairs, 1 = pairs sharing K/V loads by multicast, 0 = off.
   int pair_mode = 2;
@@ -126,14 +126,14 @@ cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* wha
   return CPATTN_OK;
 }
 
-template <int HD, bool SPLIT, int MODE>
+template <int HD, bool SPLIT, int MODE, bool VF16>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
   using Ly = cpattn::Layout<HD>;
   constexpr bool MC = MODE != 0;  // launched as clusters of two CTAs
   void (*kernel)(cpattn::PrefillParams) = MODE == 2
-                                              ? cpattn::prefill_kernel_pair2<HD, SPLIT>
-                                              : cpattn::prefill_kernel<HD, SPLIT, MODE == 1>;
-  int& grid_cap = ctx->grid_cap[HD == 256][SPLIT][MODE];
+                                              ? cpattn::prefill_kernel_pair2<HD, SPLIT, VF16>
+                                              : cpattn::prefill_kernel<HD, SPLIT, MODE == 1, VF16>;
+  int& grid_cap = ctx->grid_cap[HD == 256][SPLIT][MODE][VF16];
   if (grid_cap == 0) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Ly::SMEM_BYTES);
@@ -210,27 +210,30 @@ int pack_block_tokens(const cpattn_ctx* ctx, int32_t num_seqs, const int32_t* ch
   return kBQ / G;
 }
 
+template <int HD, bool VF16>
+cpattn_status dispatch_prefill_hd(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st,
+                                  bool split, int mode) {
+  if (mode == 2) return split ? launch_prefill<HD, true, 2, VF16>(ctx, prm, st)
+                              : launch_prefill<HD, false, 2, VF16>(ctx, prm, st);
+  if (mode == 1) return split ? launch_prefill<HD, true, 1, VF16>(ctx, prm, st)
+                              : launch_prefill<HD, false, 1, VF16>(ctx, prm, st);
+  return split ? launch_prefill<HD, true, 0, VF16>(ctx, prm, st)
+               : launch_prefill<HD, false, 0, VF16>(ctx, prm, st);
+}
+
 cpattn_status dispatch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st,
                                bool packed) {
   const int HD = ctx->cfg.head_dim;
   const bool split = ctx->cfg.fast_p == 0;
+  const bool vf16 = ctx->cfg.v_cache_f16 != 0;
   // Pair CTAs on adjacent q heads of one kv head when the group size allows
   // (packed units hold a whole group already: one CTA each).
   const int mode = (!packed && prm->group % 2 == 0) ? ctx->pair_mode : 0;
-  if (HD == 256) {
-    if (mode == 2) return split ? launch_prefill<256, true, 2>(ctx, prm, st)
-                                : launch_prefill<256, false, 2>(ctx, prm, st);
-    if (mode == 1) return split ? launch_prefill<256, true, 1>(ctx, prm, st)
-                                : launch_prefill<256, false, 1>(ctx, prm, st);
-    return split ? launch_prefill<256, true, 0>(ctx, prm, st)
-                 : launch_prefill<256, false, 0>(ctx, prm, st);
-  }
-  if (mode == 2) return split ? launch_prefill<128, true, 2>(ctx, prm, st)
-                              : launch_prefill<128, false, 2>(ctx, prm, st);
-  if (mode == 1) return split ? launch_prefill<128, true, 1>(ctx, prm, st)
-                              : launch_prefill<128, false, 1>(ctx, prm, st);
-  return split ? launch_prefill<128, true, 0>(ctx, prm, st)
-               : launch_prefill<128, false, 0>(ctx, prm, st);
+  if (HD == 256)
+    return vf16 ? dispatch_prefill_hd<256, true>(ctx, prm, st, split, mode)
+                : dispatch_prefill_hd<256, false>(ctx, prm, st, split, mode);
+  return vf16 ? dispatch_prefill_hd<128, true>(ctx, prm, st, split, mode)
+              : dispatch_prefill_hd<128, false>(ctx, prm, st, split, mode);
 }
 
 // Combine the split-KV pieces of every split row block into the output.
@@ -380,6 +383,7 @@ const char* cpattn_status_string(cpattn_status s) {
     case CPATTN_E_CUDA: return "CUDA error";
     case CPATTN_E_NOMEM: return "out of memory";
     case CPATTN_E_TIMEOUT: return "device-side wait timed out";
+    case CPATTN_E_RANGE: return "value outside the fp16 V cache's range";
   }
   return "unknown status";
 }
@@ -393,7 +397,8 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   *out = nullptr;
   const cpattn_config& c = *cfg;
   if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
-      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1)
+      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1 ||
+      c.v_cache_f16 < 0 || c.v_cache_f16 > 1)
     return CPATTN_E_INVALID;
   if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
   if (c.num_q_heads > 65535) return CPATTN_E_UNSUPPORTED;
@@ -499,6 +504,9 @@ cpattn_status cpattn_sync_status(cpattn_ctx* ctx, void* stream) {
       return fail(ctx, CPATTN_E_CUDA,
                   "the kernel's dynamic shared memory base was not aligned as required; "
                   "it returned without computing");
+    if ((word & 0xFF) == cpattn::kStatusRange)
+      return fail(ctx, CPATTN_E_RANGE,
+                  "a V value written to the fp16 V cache lies outside fp16's finite range");
     return fail(ctx, CPATTN_E_TIMEOUT,
                 "a bounded device wait expired (site " + std::to_string(word >> 8) + ")");
   }
@@ -521,6 +529,8 @@ cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* 
   p.v_new = static_cast<const uint4*>(v_new);
   p.k_cache = static_cast<uint4*>(k_cache);
   p.v_cache = static_cast<uint4*>(v_cache);
+  p.status = ctx->d_status;
+  p.v_f16 = c.v_cache_f16;
   p.num_seqs = num_seqs;
   p.nkv = c.num_kv_heads;
   p.P = c.num_shards;
@@ -715,6 +725,20 @@ namespace {
 
 constexpr int kNoAllocMaxDevices = 64;
 
+// The unpaired kernel of one precision form, as the allocation-free entry
+// point launches it (plain launch, no cluster).
+template <int HD, bool SPLIT, bool VF16>
+cudaError_t noalloc_attr() {
+  return cudaFuncSetAttribute(cpattn::prefill_kernel<HD, SPLIT, false, VF16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              cpattn::Layout<HD>::SMEM_BYTES);
+}
+template <int HD, bool SPLIT, bool VF16>
+void noalloc_launch(int grid, cudaStream_t st, const cpattn::PrefillParams& prm) {
+  cpattn::prefill_kernel<HD, SPLIT, false, VF16>
+      <<<grid, cpattn::kThreads, cpattn::Layout<HD>::SMEM_BYTES, st>>>(prm);
+}
+
 struct NoAllocDevice {
   bool ready = false;
   int* scratch = nullptr;  // device address of g_noalloc_scratch on this device
@@ -740,18 +764,14 @@ cpattn_status noalloc_setup(NoAllocDevice** out) {
       return CPATTN_E_CUDA;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return CPATTN_E_CUDA;
-    if (cudaFuncSetAttribute(cpattn::prefill_kernel<128, true, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             cpattn::Layout<128>::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn::prefill_kernel<128, false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             cpattn::Layout<128>::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn::prefill_kernel<256, true, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             cpattn::Layout<256>::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(cpattn::prefill_kernel<256, false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             cpattn::Layout<256>::SMEM_BYTES) != cudaSuccess)
+    if (noalloc_attr<128, true, false>() != cudaSuccess ||
+        noalloc_attr<128, false, false>() != cudaSuccess ||
+        noalloc_attr<256, true, false>() != cudaSuccess ||
+        noalloc_attr<256, false, false>() != cudaSuccess ||
+        noalloc_attr<128, true, true>() != cudaSuccess ||
+        noalloc_attr<128, false, true>() != cudaSuccess ||
+        noalloc_attr<256, true, true>() != cudaSuccess ||
+        noalloc_attr<256, false, true>() != cudaSuccess)
       return CPATTN_E_CUDA;
     d.scratch = ptr;
     d.ready = true;
@@ -782,7 +802,8 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   if (cfg == nullptr) return CPATTN_E_INVALID;
   const cpattn_config& c = *cfg;
   if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
-      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1)
+      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1 ||
+      c.v_cache_f16 < 0 || c.v_cache_f16 > 1)
     return CPATTN_E_INVALID;
   if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
   // Fixed-capacity host tables: sizes beyond them are refused, not grown.
@@ -874,13 +895,13 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   if (cudaMemsetAsync(dev->scratch, 0, sizeof(int), st) != cudaSuccess) return CPATTN_E_CUDA;
   const int grid = std::min(prm.num_units, dev->num_sms);
   const bool split = c.fast_p == 0;
-  if (HD == 256 && split)
-    cpattn::prefill_kernel<256, true, false><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
-  else if (HD == 256)
-    cpattn::prefill_kernel<256, false, false><<<grid, cpattn::kThreads, cpattn::Layout<256>::SMEM_BYTES, st>>>(prm);
-  else if (split)
-    cpattn::prefill_kernel<128, true, false><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
-  else
-    cpattn::prefill_kernel<128, false, false><<<grid, cpattn::kThreads, cpattn::Layout<128>::SMEM_BYTES, st>>>(prm);
+  const bool vf16 = c.v_cache_f16 != 0;
+  if (HD == 256) {
+    if (vf16) split ? noalloc_launch<256, true, true>(grid, st, prm) : noalloc_launch<256, false, true>(grid, st, prm);
+    else split ? noalloc_launch<256, true, false>(grid, st, prm) : noalloc_launch<256, false, false>(grid, st, prm);
+  } else {
+    if (vf16) split ? noalloc_launch<128, true, true>(grid, st, prm) : noalloc_launch<128, false, true>(grid, st, prm);
+    else split ? noalloc_launch<128, true, false>(grid, st, prm) : noalloc_launch<128, false, false>(grid, st, prm);
+  }
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_E_CUDA;
 }

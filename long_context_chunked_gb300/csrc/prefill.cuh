@@ -16,7 +16,8 @@
 //              over S's columns, epilogue O / l -> bf16 global stores.
 //   warp 8     TMA producer: Q once per unit, then K/V sub-tiles into a ring
 //              of 16 KB shared-memory slots.
-//   warp 9     TMEM allocation and the single MMA-issuing thread:
+//   warp 9     TMEM allocation and the MMA issue (the whole warp, one
+//              elected lane per instruction):
 //              S = Q K^T (both operands in shared memory) and
 //              O += P V (P from TMEM, V from shared memory).
 //   warp 10    the fused KV write (cpattn_prefill_write_kv), else idle.
@@ -26,10 +27,14 @@
 // over its S buffer, per 32-key chunk over that chunk's own 32 columns: the
 // bf16 rounding P_hi of p in the first 16 and, in the accurate mode (SPLIT),
 // the bf16 rounding P_lo of the remainder p - P_hi in the next 16; O then
-// takes two products P_hi V + P_lo V, which carries p to ~16 bits.
+// takes two products P_hi V + P_lo V, which carries p to ~16 bits.  With an
+// fp16 V cache (v_f16), cache tiles write P in fp16 instead (11-bit
+// significand) and take one product against the fp16 V tile.
 // MMAs of one thread execute in issue order, so the QK^T that next
 // overwrites that buffer (tile t+2) runs after PV_t read P_t.
 #pragma once
+
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -139,6 +144,7 @@ struct Layout {
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_QK = make_idesc_bf16(kBQ, kBKV, false);
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(kBQ, HD, true);
+  static constexpr uint32_t IDESC_PV_F16 = make_idesc_f16(kBQ, HD, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(HD + 2 * kBKV <= TMEM_COLS, "TMEM budget");
 };
@@ -312,7 +318,7 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
 // exactly once per launch.  These cache rows hold tokens >= L_b, which no
 // unit of this launch reads as keys.  16-byte vectors, consecutive lanes on
 // consecutive vectors of a row.
-template <int HD>
+template <int HD, bool VF16>
 __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane) {
   constexpr int VECS = HD * 2 / 16;  // 16-byte vectors per row
   for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
@@ -326,7 +332,12 @@ __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane)
       const long long src = ((static_cast<long long>(U.b) * p.C + U.q0 + r) * p.nkv + U.g) * HD;
       const long long dst = (head_row + static_cast<long long>(t % p.P) * p.S + t / p.P) * HD;
       const uint4 kv = reinterpret_cast<const uint4*>(p.k_new + src)[x];
-      const uint4 vv = reinterpret_cast<const uint4*>(p.v_new + src)[x];
+      uint4 vv = reinterpret_cast<const uint4*>(p.v_new + src)[x];
+      if (VF16) {
+        bool overflow = false;
+        vv = bf16x8_to_f16x8(vv, &overflow);
+        if (overflow && p.status != nullptr) atomicCAS(p.status, kStatusOk, kStatusRange);
+      }
       reinterpret_cast<uint4*>(p.k_cache_w + dst)[x] = kv;
       reinterpret_cast<uint4*>(p.v_cache_w + dst)[x] = vv;
     }
@@ -337,7 +348,7 @@ __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane)
 // Run by the whole MMA warp: control flow and operands are warp-uniform (every
 // wait's outcome is agreed by the warp), and each MMA and commit is issued by
 // one elected lane.
-template <int HD, bool SPLIT, bool MC>
+template <int HD, bool SPLIT, bool MC, bool VF16>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                          const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -369,8 +380,12 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   const uint32_t ser_phase = 0;
 #endif
 
-  // O (+)= P_w V_w, P_w from the S buffer of global tile t.
-  auto issue_pv = [&](int w, uint32_t t) {
+  // O (+)= P_w V_w, P_w from the S buffer of global tile t; F16: a tile of
+  // the fp16 V cache (one product of fp16 P and V per 16 keys).  The form is
+  // chosen once per tile: a branch between the elected MMAs of the warp
+  // would cost every MMA a reconvergence.
+  auto issue_pv_as = [&](int w, uint32_t t, auto f16tag) {
+    constexpr bool F16 = decltype(f16tag)::value;
     const uint32_t sb = t & 1u;
     if (!wwait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
     tc_fence_after();
@@ -387,8 +402,12 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
         // (e0 % 32) / 2 within the chunk's hi half; its lo half follows.
         const int e0 = j * Ly::VROWS + kk * 16;
         const uint32_t pa = p_tmem + 32 * (e0 >> 5) + ((e0 & 31) >> 1);
-        mma_ts(tmem, pa, bd, Ly::IDESC_PV, (w | j | kk) != 0);
-        if (SPLIT) mma_ts(tmem, pa + 16, bd, Ly::IDESC_PV, 1u);
+        if (F16) {
+          mma_ts(tmem, pa, bd, Ly::IDESC_PV_F16, (w | j | kk) != 0);
+        } else {
+          mma_ts(tmem, pa, bd, Ly::IDESC_PV, (w | j | kk) != 0);
+          if (SPLIT) mma_ts(tmem, pa + 16, bd, Ly::IDESC_PV, 1u);
+        }
       }
       serialize();
       release_slot(bar(Ly::B_SLOTEMPTY + rp.slot));
@@ -396,6 +415,12 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
     }
     mma_commit(bar(Ly::B_ODONE + static_cast<int>(t & 1u)));
     return true;
+  };
+  auto issue_pv = [&](const Unit& U, int w, uint32_t t) {
+    if constexpr (VF16) {
+      if (U.v0 + w < U.n_cache) return issue_pv_as(w, t, std::true_type{});
+    }
+    return issue_pv_as(w, t, std::false_type{});
   };
 
   for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
@@ -428,13 +453,13 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
       if (!ok) break;
       mma_commit(bar(Ly::B_SFULL + sb));
       if (v == U.n_tiles - 1) mma_commit(bar(Ly::B_QEMPTY));
-      if (v >= 1 && !issue_pv(v - 1, tile_ctr - 1)) {
+      if (v >= 1 && !issue_pv(U, v - 1, tile_ctr - 1)) {
         ok = false;
         break;
       }
       ++tile_ctr;
     }
-    if (ok) ok = issue_pv(U.n_tiles - 1, tile_ctr - 1);
+    if (ok) ok = issue_pv(U, U.n_tiles - 1, tile_ctr - 1);
   }
   // Every MMA issued must complete before TMEM is released.
   mma_commit(bar(Ly::B_DRAIN));
@@ -461,7 +486,7 @@ __device__ __forceinline__ uint32_t causal_word(int lim, int q) {
 // PAIR2: the CTA is one of a pair whose leader issues 2-SM MMAs; S, P and O
 // of this CTA's 128 rows sit in its own TMEM exactly as in a single CTA, but
 // "P ready" goes to the leader's barrier, one arrival per warp.
-template <int HD, bool SPLIT, bool PAIR2 = false>
+template <int HD, bool SPLIT, bool PAIR2, bool VF16>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                              const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -600,7 +625,10 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       const float2 minus1 = make_float2(-1.f, -1.f);
       float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
       {
-        auto chunk_exp = [&](const uint32_t (&x)[32], int q) {
+        // F16: a tile of an fp16 V cache takes P in fp16 (11-bit significand,
+        // one P.V product); otherwise P_hi in bf16 and, accurate mode, P_lo.
+        auto chunk_exp = [&](const uint32_t (&x)[32], int q, auto f16tag) {
+          constexpr bool F16 = decltype(f16tag)::value;
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -609,19 +637,33 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
                 negm2);
             const float2 pab = make_float2(ex2_approx(y.x), ex2_approx(y.y));
             if (i & 1) lsb = __fadd2_rn(lsb, pab); else lsa = __fadd2_rn(lsa, pab);
-            hi[i] = pack_bf16x2(pab.x, pab.y);
-            if (SPLIT) {
-              const float2 hf = make_float2(__uint_as_float(hi[i] << 16),
-                                            __uint_as_float(hi[i] & 0xFFFF0000u));
-              const float2 res = __ffma2_rn(hf, minus1, pab);
-              lo[i] = pack_bf16x2(res.x, res.y);
+            if (F16) {
+              hi[i] = pack_f16x2(pab.x, pab.y);
+            } else {
+              hi[i] = pack_bf16x2(pab.x, pab.y);
+              if (SPLIT) {
+                const float2 hf = make_float2(__uint_as_float(hi[i] << 16),
+                                              __uint_as_float(hi[i] & 0xFFFF0000u));
+                const float2 res = __ffma2_rn(hf, minus1, pab);
+                lo[i] = pack_bf16x2(res.x, res.y);
+              }
             }
           }
           tmem_st16(s_tmem + 32 * q, hi);
-          if (SPLIT) tmem_st16(s_tmem + 32 * q + 16, lo);
+          if (SPLIT && !F16) tmem_st16(s_tmem + 32 * q + 16, lo);
         };
+        bool f16_done = false;
+        if constexpr (VF16) {
+          if (in_cache) {
 #pragma unroll
-        for (int c = 0; c < CH; ++c) chunk_exp(rr[c], c);
+            for (int c = 0; c < CH; ++c) chunk_exp(rr[c], c, std::true_type{});
+            f16_done = true;
+          }
+        }
+        if (!f16_done) {
+#pragma unroll
+          for (int c = 0; c < CH; ++c) chunk_exp(rr[c], c, std::false_type{});
+        }
       }
       l = l * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
@@ -734,7 +776,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 }
 
 // ------------------------------------------------------------------ kernel
-template <int HD, bool SPLIT, bool MC>
+template <int HD, bool SPLIT, bool MC, bool VF16>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -783,13 +825,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
 
   if (warp < kProducerWarp) {
-    softmax_role<HD, SPLIT>(p, sbase, tmem, wait);
+    softmax_role<HD, SPLIT, false, VF16>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<HD, MC>(p, sbase, wait);
   } else if (warp == kWriterWarp) {
-    if (p.k_cache_w != nullptr) kv_write_lanes<HD>(p, lane);
+    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16>(p, lane);
   } else {
-    mma_role<HD, SPLIT, MC>(p, sbase, tmem, wait);
+    mma_role<HD, SPLIT, MC, VF16>(p, sbase, tmem, wait);
   }
   __syncwarp();
   tc_fence_before();

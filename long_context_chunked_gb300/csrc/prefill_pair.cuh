@@ -45,6 +45,7 @@ struct PairLayout {
   static constexpr int BOX = 8192;             // bytes per 64 x 64 box
   static constexpr uint32_t IDESC_QK = make_idesc_bf16(2 * kBQ, kBKV, false);
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(2 * kBQ, HD, true);
+  static constexpr uint32_t IDESC_PV_F16 = make_idesc_f16(2 * kBQ, HD, true);
   static constexpr uint32_t P_ARRIVALS = 2 * kSoftmaxThreads / 32;
   static_assert(VCH * VRG * BOX == Layout<HD>::SUB, "V slot = 16 KB");
   static_assert(2 * BOX == Layout<HD>::SUB, "K slot = two chunks of 64 rows");
@@ -159,7 +160,7 @@ __device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint
 // Leader CTA only, the whole MMA warp: control flow and operands are
 // warp-uniform (every wait's outcome is agreed by the warp), and each MMA and
 // commit is issued by one elected lane.
-template <int HD, bool SPLIT>
+template <int HD, bool SPLIT, bool VF16>
 __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t sbase,
                                                uint32_t tmem, const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -187,8 +188,12 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
   const uint32_t ser_phase = 0;
 #endif
 
-  // O (+)= P_w V_w over both CTAs' rows, P_w from the S buffer of tile t.
-  auto issue_pv = [&](int w, uint32_t t) {
+  // O (+)= P_w V_w over both CTAs' rows, P_w from the S buffer of tile t;
+  // F16: a tile of the fp16 V cache (one product of fp16 P and V per 16
+  // keys).  The form is chosen once per tile: a branch between the elected
+  // MMAs of the warp would cost every MMA a reconvergence.
+  auto issue_pv_as = [&](int w, uint32_t t, auto f16tag) {
+    constexpr bool F16 = decltype(f16tag)::value;
     const uint32_t sb = t & 1u;
     if (!wwait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
     tc_fence_after();
@@ -204,8 +209,12 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
         const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, Pl::VR * 128, 1024);
         const int e0 = j * Pl::VR + kk * 16;
         const uint32_t pa = p_tmem + 32 * (e0 >> 5) + ((e0 & 31) >> 1);
-        mma2_ts(tmem, pa, bd, Pl::IDESC_PV, (w | j | kk) != 0);
-        if (SPLIT) mma2_ts(tmem, pa + 16, bd, Pl::IDESC_PV, 1u);
+        if (F16) {
+          mma2_ts(tmem, pa, bd, Pl::IDESC_PV_F16, (w | j | kk) != 0);
+        } else {
+          mma2_ts(tmem, pa, bd, Pl::IDESC_PV, (w | j | kk) != 0);
+          if (SPLIT) mma2_ts(tmem, pa + 16, bd, Pl::IDESC_PV, 1u);
+        }
       }
       serialize();
       mma2_commit_mc(bar(Ly::B_SLOTEMPTY + rp.slot), 0x3);
@@ -213,6 +222,12 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
     }
     mma2_commit_mc(bar(Ly::B_ODONE + static_cast<int>(t & 1u)), 0x3);
     return true;
+  };
+  auto issue_pv = [&](const Unit& U, int w, uint32_t t) {
+    if constexpr (VF16) {
+      if (U.v0 + w < U.n_cache) return issue_pv_as(w, t, std::true_type{});
+    }
+    return issue_pv_as(w, t, std::false_type{});
   };
 
   for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
@@ -249,13 +264,13 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
       if (!ok) break;
       mma2_commit_mc(bar(Ly::B_SFULL + sb), 0x3);
       if (v == U.n_tiles - 1) mma2_commit_mc(bar(Ly::B_QEMPTY), 0x3);
-      if (v >= 1 && !issue_pv(v - 1, tile_ctr - 1)) {
+      if (v >= 1 && !issue_pv(U, v - 1, tile_ctr - 1)) {
         ok = false;
         break;
       }
       ++tile_ctr;
     }
-    if (ok) ok = issue_pv(U.n_tiles - 1, tile_ctr - 1);
+    if (ok) ok = issue_pv(U, U.n_tiles - 1, tile_ctr - 1);
   }
   // Every MMA issued must complete before either CTA releases its TMEM.
   mma2_commit_mc(bar(Ly::B_DRAIN), 0x1);
@@ -266,7 +281,7 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
 // Launched with clusters of two CTAs; CTA 2k + r runs units u = 2k + r +
 // m * gridDim.x, so the pair always holds q heads 2i and 2i + 1 of the same
 // row block (the host launches it only when the group size is even).
-template <int HD, bool SPLIT>
+template <int HD, bool SPLIT, bool VF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel_pair2(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
@@ -316,13 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
 
   if (warp < kProducerWarp) {
-    softmax_role<HD, SPLIT, true>(p, sbase, tmem, wait);
+    softmax_role<HD, SPLIT, true, VF16>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
   } else if (warp == kWriterWarp) {
-    if (p.k_cache_w != nullptr) kv_write_lanes<HD>(p, lane);
+    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16>(p, lane);
   } else if (warp == kMmaWarp && rank == 0) {
-    mma_role_pair2<HD, SPLIT>(p, sbase, tmem, wait);
+    mma_role_pair2<HD, SPLIT, VF16>(p, sbase, tmem, wait);
   }
   __syncwarp();
   tc_fence_before();

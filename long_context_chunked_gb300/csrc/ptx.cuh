@@ -79,7 +79,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluste
 }
 
 // Device status word codes (written by the first role that gives up).
-enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusLayout = 2 };
+enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusLayout = 2, kStatusRange = 3 };
 
 // A wait with a wall-clock limit.  On expiry it records the site in the
 // device status word, raises the CTA-wide abort flag and returns false; a
@@ -400,6 +400,13 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_m
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
+// The same with A and B in fp16 (format code 0).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                  // D format: fp32
+         | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand: start
 // address, leading- and stride-dimension byte offsets (both /16), the
@@ -426,6 +433,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   // cvt packs its first source into the upper half.
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two fp32 values rounded to nearest-even fp16, lo in the lower half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Eight bf16 values (one 16-byte vector) as eight fp16 values, rounded to
+// nearest-even (bf16 -> fp32 is exact); *overflow is set when a result is
+// infinite or NaN, i.e. the value lies outside fp16's finite range.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool* overflow) {
+  auto conv = [&](uint32_t w) {
+    const uint32_t h = pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    // exponent field all ones in either half: inf or NaN
+    if ((h & 0x7C00u) == 0x7C00u || (h & 0x7C000000u) == 0x7C000000u) *overflow = true;
+    return h;
+  };
+  return make_uint4(conv(v.x), conv(v.y), conv(v.z), conv(v.w));
 }
 
 }  // namespace cpattn

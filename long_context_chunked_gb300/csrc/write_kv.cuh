@@ -6,10 +6,13 @@
 // HBM-bound copy.  One thread moves one 16-byte vector of K and the same
 // vector of V; consecutive threads cover consecutive vectors of one source
 // row, so loads and stores are fully coalesced within each HD*2-byte row.
+// An fp16 V cache (v_f16) receives each V value converted from bf16 (exact
+// inside fp16's range); a value outside it sets kStatusRange in *status.
 #pragma once
 
 #include <cstdint>
 
+#include "ptx.cuh"
 #include "walk.cuh"
 
 namespace cpattn {
@@ -19,6 +22,8 @@ struct WriteKvParams {
   const uint4* v_new;
   uint4* k_cache;
   uint4* v_cache;
+  int* status;                            // device status word (range errors)
+  int v_f16;                              // V cache in fp16
   int num_seqs, nkv, P, S, C;
   int vec_per_row;                        // HD * 2 / 16
   long long total_vecs;                   // sum_b c_b * NKV * vec_per_row
@@ -48,7 +53,12 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ W
         (static_cast<long long>(b * p.nkv + g) * p.P + (t % p.P)) * p.S + (t / p.P);
     const long long dst = dst_row * p.vec_per_row + vec;
     const uint4 kv = __ldg(p.k_new + src);
-    const uint4 vv = __ldg(p.v_new + src);
+    uint4 vv = __ldg(p.v_new + src);
+    if (p.v_f16) {
+      bool overflow = false;
+      vv = bf16x8_to_f16x8(vv, &overflow);
+      if (overflow && p.status != nullptr) atomicCAS(p.status, kStatusOk, kStatusRange);
+    }
     p.k_cache[dst] = kv;
     p.v_cache[dst] = vv;
   }

@@ -42,13 +42,15 @@ def _scatter(cache: np.ndarray, b: int, positions: np.ndarray, rows: np.ndarray,
 
 
 def write_kv_ref(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
-                 cache_lens: Sequence[int], chunk_lens: Sequence[int], chunk: int) -> None:
+                 cache_lens: Sequence[int], chunk_lens: Sequence[int], chunk: int,
+                 v_f16: bool = False) -> None:
     """In-place KV write of one prefill step (operands as uint16 bit patterns).
 
     k_cache, v_cache: [B, NKV, P, S, HD];  k_new, v_new: [B*C, NKV, HD] in
     token order.  For each sequence b, the valid chunk tokens i < c_b go to
     token position t = L_b + i.  Pad rows (i >= c_b) and every other cache
-    row are left untouched.
+    row are left untouched.  v_f16: the V cache holds binary16, and each bf16
+    value of v_new is stored as ``bf16_to_f16_bits`` of it.
     """
     B, _, P, S, _ = k_cache.shape
     for b in range(B):
@@ -58,7 +60,7 @@ def write_kv_ref(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_
         pos = np.arange(L, L + c)
         src = slice(b * chunk, b * chunk + c)
         _scatter(k_cache, b, pos, k_new[src], P, S)
-        _scatter(v_cache, b, pos, v_new[src], P, S)
+        _scatter(v_cache, b, pos, bf16_to_f16_bits(v_new[src]) if v_f16 else v_new[src], P, S)
 
 
 def build_striped_cache(logical: Sequence[np.ndarray], num_kv_heads: int, P: int, S: int,
@@ -95,3 +97,21 @@ def bf16_bits(x) -> np.ndarray:
 def bits_to_f64(u16: np.ndarray) -> np.ndarray:
     """Decode bf16 bit patterns (uint16) to float64 exactly."""
     return (np.asarray(u16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_to_f16_bits(u16: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> IEEE 754 binary16 bit patterns of the same values.
+
+    The bf16 value (exact in float32) is rounded to the nearest binary16,
+    ties to even, as IEEE 754 defines conversion to a narrower format:
+    exact for normal values within binary16's range, rounded below 2^-14
+    (subnormals), +-inf beyond 65504 + half an ulp.
+    """
+    f32 = (np.asarray(u16).astype(np.uint32) << 16).view(np.float32)
+    with np.errstate(over="ignore"):
+        return f32.astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f64(u16: np.ndarray) -> np.ndarray:
+    """Decode binary16 bit patterns (uint16) to float64 exactly."""
+    return np.asarray(u16, dtype=np.uint16).view(np.float16).astype(np.float64)

@@ -72,7 +72,8 @@ class DeviceCase:
         self.k_new = Guarded(case.k_new_bits.shape, case.k_new_bits)
         self.v_new = Guarded(case.v_new_bits.shape, case.v_new_bits)
         self.k_cache = Guarded(case.k_cache_bits.shape, case.k_cache_bits)
-        self.v_cache = Guarded(case.v_cache_bits.shape, case.v_cache_bits)
+        self.v_cache = Guarded(case.v_cache_bits.shape, case.v_cache_bits,
+                               dtype=torch.float16 if case.v_f16 else torch.bfloat16)
         self.out = Guarded((w.tokens, w.num_q_heads, w.head_dim))
         self.lse = torch.full((w.tokens, w.num_q_heads), float("nan"), dtype=torch.float32,
                               device="cuda")

@@ -30,9 +30,12 @@ class Case:
     k_new_bits: np.ndarray    # [T, NKV, HD]
     v_new_bits: np.ndarray
     k_cache_bits: np.ndarray  # [B, NKV, P, S, HD] striped, holes = POISON_BITS
-    v_cache_bits: np.ndarray
+    v_cache_bits: np.ndarray  # bf16, or binary16 when v_f16
+    v_f16: bool = False
 
     def f64(self, name: str) -> np.ndarray:
+        if name == "v_cache" and self.v_f16:
+            return oracle.f16_bits_to_f64(self.v_cache_bits)
         return oracle.bits_to_f64(getattr(self, name + "_bits"))
 
     def oracle_full(self, threads: int = 1):
@@ -43,20 +46,25 @@ class Case:
 
     def oracle_rows(self, samples):
         w = self.w
+        vc = self.f64("v_cache") if self.v_f16 else self.v_cache_bits
         return oracle.attend_rows_ref(self.q_bits, self.k_new_bits, self.v_new_bits,
-                                      self.k_cache_bits, self.v_cache_bits, w.cache_lens,
+                                      self.k_cache_bits, vc, w.cache_lens,
                                       w.chunk_lens, w.chunk, w.scale, samples)
 
 
-def make_case(w: Workload, hole_bits=POISON_BITS) -> Case:
+def make_case(w: Workload, hole_bits=POISON_BITS, v_f16: bool = False) -> Case:
+    """v_f16: the V cache in binary16 (its bf16 values converted as the fp16
+    cache write converts them; the oracle then reads V as stored)."""
     inp = generate(w)
     kc = oracle.build_striped_cache([oracle.bf16_bits(x) for x in inp.k_cache], w.num_kv_heads,
                                     w.shards, w.shard_capacity, w.head_dim, hole_bits)
     vc = oracle.build_striped_cache([oracle.bf16_bits(x) for x in inp.v_cache], w.num_kv_heads,
                                     w.shards, w.shard_capacity, w.head_dim, hole_bits)
+    if v_f16:
+        vc = oracle.bf16_to_f16_bits(vc)
     return Case(w=w, inputs=inp, q_bits=oracle.bf16_bits(inp.q),
                 k_new_bits=oracle.bf16_bits(inp.k_new), v_new_bits=oracle.bf16_bits(inp.v_new),
-                k_cache_bits=kc, v_cache_bits=vc)
+                k_cache_bits=kc, v_cache_bits=vc, v_f16=v_f16)
 
 
 def sample_rows(w: Workload, n: int, seed: int = 1234):

@@ -278,3 +278,55 @@ def pin_large_logits():
     o, l = oracle.attend_ref(q, kn, vn, kcs, vcs, [3], [1], 1, 1000.0)
     _close(o[0, 0], vc[1, 0], 1e-12, "hard max picks the largest key")
     _close(l[0, 0], 20000.0, 1e-9, "LSE of a hard max")
+
+
+def pin_f16_conversion():
+    """bf16 -> binary16 (IEEE 754 conversion to a narrower format, round to
+    nearest even) over every bf16 pattern, against an integer restatement:
+    values in binary16's normal range keep their value exactly; below 2^-14
+    the result is the nearest multiple of 2^-24 (ties to even, Python's
+    round); from 65520 up it is infinite."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    x = oracle.bits_to_f64(bits)
+    h = oracle.bf16_to_f16_bits(bits)
+    y = oracle.f16_bits_to_f64(h)
+    fin = np.isfinite(x)
+    ax = np.abs(x)
+    normal = fin & (ax >= 2.0 ** -14) & (ax <= 65504.0)
+    assert np.array_equal(y[normal], x[normal]), "normal range is exact"
+    sub = fin & (ax < 2.0 ** -14)
+    for xi, hi in zip(x[sub], h[sub]):
+        n = round(abs(float(xi)) * 2.0 ** 24)       # ties to even
+        sign = 0x8000 if math.copysign(1.0, float(xi)) < 0 else 0
+        assert int(hi) == (sign | n), (xi, hex(int(hi)))
+    big = fin & (ax >= 65520.0)
+    assert np.all(np.isinf(y[big])) and np.array_equal(np.sign(y[big]), np.sign(x[big]))
+    # binary16 decode at fixed patterns
+    fixed = {0x3C00: 1.0, 0xC000: -2.0, 0x7BFF: 65504.0, 0x0001: 2.0 ** -24, 0x0400: 2.0 ** -14,
+             0x3555: 0.333251953125, 0xFC00: -math.inf}
+    for b, v in fixed.items():
+        assert oracle.f16_bits_to_f64(np.array([b], dtype=np.uint16))[0] == v, hex(b)
+
+
+def pin_write_kv_f16():
+    """An fp16 V cache receives each written V value converted; K and the
+    untouched rows are as in the bf16 write."""
+    w = small("wkv16", (0, 5, 17), (4, 0, 6), 6, nq=2, nkv=2, hd=4, shards=4, shard_capacity=6)
+    rng = np.random.default_rng(3)
+    kn = rng.integers(0, 0x7F00, size=(w.tokens, 2, 4), dtype=np.uint16)
+    vn = rng.integers(0, 0x4700, size=(w.tokens, 2, 4), dtype=np.uint16)  # |v| < 2^15
+    kc = np.full((3, 2, 4, 6, 4), 0x1234, dtype=np.uint16)
+    vc = kc.copy()
+    kc2, vc2 = kc.copy(), vc.copy()
+    oracle.write_kv_ref(kc, vc, kn, vn, w.cache_lens, w.chunk_lens, w.chunk, v_f16=True)
+    oracle.write_kv_ref(kc2, vc2, kn, vn, w.cache_lens, w.chunk_lens, w.chunk)
+    assert np.array_equal(kc, kc2), "K is written as in the bf16 cache"
+    for b in range(3):
+        for i in range(w.chunk_lens[b]):
+            t = w.cache_lens[b] + i
+            got = oracle.f16_bits_to_f64(vc[b, :, t % 4, t // 4, :])
+            want = oracle.bits_to_f64(vn[b * 6 + i])
+            small_ = np.abs(want) < 2.0 ** -14
+            assert np.array_equal(got[~small_], want[~small_]), (b, i)
+            assert np.all(np.abs(got[small_] - want[small_]) <= 2.0 ** -25), (b, i)
+    assert np.array_equal(vc == 0x1234, vc2 == 0x1234), "the same rows are written"

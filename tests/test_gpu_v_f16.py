@@ -1,0 +1,171 @@
+"""fp16 V cache on the GPU against the fp64 oracle.
+
+With cpattn_config.v_cache_f16 the KV write stores each V value converted to
+binary16, and prefill takes P in fp16 for cache tiles: one P.V product per 16
+keys instead of the bf16 hi + lo pair.  The oracle reads V as stored.  Bar as
+everywhere: max |diff| <= 1e-2 and relative RMS <= 2e-3.  Checked over both
+head dims, paired / multicast / unpaired CTAs, GQA packing, split-KV, the
+fused KV write, fast_p on and off, the full-size workloads on sampled rows,
+the bit-exact fp16 cache write and its range error."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import long_context_chunked_gb300 as cp
+from gpu_helpers import DeviceCase, compare, to_f64
+from helpers import make_case, sample_rows
+from workloads import CTX_8K, CTX_32K, CTX_128K, VARLEN, small
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    small("f16a", (0, 1000, 129, 3000), (300, 1, 256, 77), 320, nq=8, nkv=2, hd=128, shards=4,
+          shard_capacity=800, seed=141),
+    small("f16b", (5000, 1), (130, 384), 384, nq=4, nkv=1, hd=256, shards=8, seed=142),
+    small("f16c", (2000,), (200,), 256, nq=3, nkv=3, hd=128, shards=3, seed=143),  # unpaired
+    small("f16d", (20000, 0, 9000), (1, 5, 64), 64, nq=32, nkv=2, hd=256, shards=8,
+          seed=144),  # GQA-packed
+]
+
+
+def _check(w, dc, case, fast_p=False):
+    ref, ref_lse = case.oracle_full()
+    v = dc.valid_rows()
+    out = to_f64(dc.out.bits())
+    if fast_p:
+        # Current-chunk tiles then take P rounded once to bf16, whose error
+        # floor (~2.2e-3 relative RMS) is above the bar: fast_p's own bound.
+        res = compare(out[v], ref[v], f"{w.name} fast_p", max_abs_bar=2e-2, rel_bar=3.5e-3)
+    else:
+        res = compare(out[v], ref[v], w.name)
+    lse = dc.lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse[v] - ref_lse[v])) < 2e-3, "LSE"
+    pad = ~v
+    if pad.any():
+        assert np.all(dc.out.bits()[pad] == np.uint16(0x7F7F)), "pad rows written"
+    assert dc.guards_intact(), "write outside a buffer"
+    return res
+
+
+@pytest.mark.parametrize("fast_p", [False, True], ids=["accurate", "fast_p"])
+@pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
+def test_parity(w, fast_p):
+    case = make_case(w, v_f16=True)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w, fast_p=fast_p, v_cache_f16=True)
+    dc.prefill(ctx)
+    _check(w, dc, case, fast_p)
+
+
+@pytest.mark.parametrize("mode", ["mma2", "multicast", "none"])
+def test_pairing_modes(mode, monkeypatch):
+    monkeypatch.setenv("CPATTN_PAIRING", mode)
+    w = CASES[0]
+    case = make_case(w, v_f16=True)
+    dc = DeviceCase(case)
+    dc.prefill(cp.Context.for_workload(w, v_cache_f16=True))
+    _check(w, dc, case)
+
+
+@pytest.mark.parametrize("t", [1, 3])
+def test_split_kv(t):
+    w = CASES[1]
+    case = make_case(w, v_f16=True)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w, v_cache_f16=True)
+    need, _ = ctx.splitkv_workspace(w.cache_lens, w.chunk_lens, t)
+    ws = torch.empty(max(need // 4, 64), dtype=torch.float32, device="cuda")
+    ctx.set_splitkv(ws, t)
+    dc.prefill(ctx)
+    _check(w, dc, case)
+
+
+def test_more_accurate_than_single_bf16_p():
+    """fp16 P on cache tiles carries 11 significand bits: on a cache-heavy
+    case its error stays at the accurate mode's level, below the
+    single-bf16-P (fast_p, bf16 cache) error."""
+    w = small("f16acc", (6000,), (256,), 256, nq=4, nkv=2, hd=128, shards=8, seed=145)
+    errs = {}
+    for name, f16, fast in (("f16", True, False), ("bf16_fast", False, True)):
+        case = make_case(w, v_f16=f16)
+        dc = DeviceCase(case)
+        dc.prefill(cp.Context.for_workload(w, fast_p=fast, v_cache_f16=f16))
+        ref, _ = case.oracle_full()
+        v = dc.valid_rows()
+        errs[name] = compare(to_f64(dc.out.bits())[v], ref[v], name, rel_bar=3e-3)[1]
+    assert errs["f16"] < 0.9 * errs["bf16_fast"], errs
+
+
+def test_write_kv_bit_exact():
+    w = CASES[0]
+    case = make_case(w, v_f16=True)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w, v_cache_f16=True)
+    kc_ref, vc_ref = case.k_cache_bits.copy(), case.v_cache_bits.copy()
+    oracle.write_kv_ref(kc_ref, vc_ref, case.k_new_bits, case.v_new_bits, w.cache_lens,
+                        w.chunk_lens, w.chunk, v_f16=True)
+    ctx.write_kv(w.cache_lens, w.chunk_lens, dc.k_new.t, dc.v_new.t, dc.k_cache.t, dc.v_cache.t)
+    assert ctx.sync_status() == cp.OK, ctx.last_error()
+    assert np.array_equal(dc.k_cache.bits(), kc_ref), "K cache differs from the oracle scatter"
+    assert np.array_equal(dc.v_cache.bits(), vc_ref), "V cache differs from the oracle scatter"
+    assert dc.guards_intact()
+
+
+def test_fused_write_kv():
+    w = CASES[0]
+    case = make_case(w, v_f16=True)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w, v_cache_f16=True)
+    kc_ref, vc_ref = case.k_cache_bits.copy(), case.v_cache_bits.copy()
+    oracle.write_kv_ref(kc_ref, vc_ref, case.k_new_bits, case.v_new_bits, w.cache_lens,
+                        w.chunk_lens, w.chunk, v_f16=True)
+    ctx.prefill_write_kv(w.cache_lens, w.chunk_lens, dc.q.t, dc.k_new.t, dc.v_new.t,
+                         dc.k_cache.t, dc.v_cache.t, dc.out.t, dc.lse)
+    assert ctx.sync_status() == cp.OK, ctx.last_error()
+    _check(w, dc, case)
+    assert np.array_equal(dc.k_cache.bits(), kc_ref), "K cache differs from the oracle scatter"
+    assert np.array_equal(dc.v_cache.bits(), vc_ref), "V cache differs from the oracle scatter"
+
+
+def test_range_error_reported():
+    """A V value beyond binary16's range (1e5) written to an fp16 cache makes
+    the next status read CPATTN_E_RANGE; the status word is then clear."""
+    w = small("f16rng", (100,), (40,), 64, nq=2, nkv=1, hd=128, shards=2, seed=146)
+    case = make_case(w, v_f16=True)
+    case.v_new_bits[7, 0, 5] = np.uint16(0x47C3)  # bf16 99840
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w, v_cache_f16=True)
+    ctx.write_kv(w.cache_lens, w.chunk_lens, dc.k_new.t, dc.v_new.t, dc.k_cache.t, dc.v_cache.t)
+    assert ctx.sync_status() == cp.E_RANGE
+    assert ctx.sync_status() == cp.OK
+    # The same write into a bf16 cache is a plain copy: no error.
+    ctx16 = cp.Context.for_workload(w)
+    dc2 = DeviceCase(make_case(w))
+    ctx16.write_kv(w.cache_lens, w.chunk_lens, dc.k_new.t, dc.v_new.t, dc2.k_cache.t,
+                   dc2.v_cache.t)
+    assert ctx16.sync_status() == cp.OK
+
+
+FULL = [CTX_8K, CTX_32K, CTX_128K, VARLEN]
+
+
+@pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
+def test_full_size_sampled(w):
+    """The benchmarked workloads at full size with the fp16 V cache, in the
+    launch configuration the benchmark times: sampled rows against the oracle
+    (first/last rows of each sequence and q-block edges included)."""
+    case = make_case(w, v_f16=True)
+    dc = DeviceCase(case)
+    ctx = cp.Context.for_workload(w, v_cache_f16=True)
+    dc.prefill(ctx)
+    samples = sample_rows(w, 48, seed=w.seed)
+    ref, ref_lse = case.oracle_rows(samples)
+    out = to_f64(dc.out.bits())
+    got = np.stack([out[t, h] for t, h in samples])
+    compare(got, ref, w.name)
+    lse = dc.lse.cpu().numpy()
+    assert np.max(np.abs(np.array([lse[t, h] for t, h in samples]) - ref_lse)) < 2e-3
+    v = dc.valid_rows()
+    assert np.all(np.isfinite(out[v])), "non-finite output"
+    assert dc.guards_intact()
