@@ -391,7 +391,7 @@ PAGES_TTFT_MS = {8192: 2.55, 16384: 6.29, 32768: 17.23, 65536: 53.05, 131072: 18
                  262144: 661.0, 1048576: 9769.0}
 
 
-def run_cumulative(contexts, fast_p=False, seed=7):
+def run_cumulative(contexts, fast_p=False, seed=7, v_f16=False):
     """Every 4096-token chunk of one request of each context length, back to
     back on one stream: write the chunk into the striped cache, then prefill it
     against everything before it.  Prints one JSON line per context."""
@@ -407,8 +407,8 @@ def run_cumulative(contexts, fast_p=False, seed=7):
     for n in contexts:
         S = (n + P - 1) // P
         kc = torch.zeros((1, NKV, P, S, HD), dtype=torch.bfloat16, device=dev)
-        vc = torch.zeros_like(kc)
-        ctx = cp.Context(NQ, NKV, HD, P, S, C, 0.0, fast_p)
+        vc = torch.zeros_like(kc, dtype=torch.float16 if v_f16 else torch.bfloat16)
+        ctx = cp.Context(NQ, NKV, HD, P, S, C, 0.0, fast_p, v_f16)
         chunks = n // C
 
         def request():
@@ -429,7 +429,8 @@ def run_cumulative(contexts, fast_p=False, seed=7):
         flops = sum(4 * HD * NQ * (C * k * C + C * (C + 1) // 2) for k in range(chunks))
         print(json.dumps({"mode": "cumulative_prefill", "context": n, "chunks": chunks,
                           "request_ms": round(ms, 3), "tflops": round(flops / ms / 1e9, 1),
-                          "precision": "fast_p" if fast_p else "accurate P",
+                          "precision": precision_label(fast_p, v_f16),
+                          "v_cache": "f16" if v_f16 else "bf16",
                           "pages_tpu_v7x8_fused_ring_ms": PAGES_TTFT_MS.get(n)}), flush=True)
         del kc, vc, ctx
 
@@ -444,7 +445,7 @@ SPLITKV_CASES = [
 ]
 
 
-def run_splitkv(fast_p=False, reps=20, seed=11):
+def run_splitkv(fast_p=False, reps=20, seed=11, v_f16=False):
     """Each small-chunk workload fused (one launch) and split-KV (automatic
     plan: pieces + merge; the same single launch when the plan cuts nothing),
     alternating rep by rep, L2 flushed before every rep, CUDA events on the
@@ -465,9 +466,10 @@ def run_splitkv(fast_p=False, reps=20, seed=11):
         kn = torch.randn(B * C, NKV, HD, generator=gen).to(torch.bfloat16).to(dev)
         vn = torch.randn(B * C, NKV, HD, generator=gen).to(torch.bfloat16).to(dev)
         kc = torch.randn(B, NKV, P, S, HD, generator=gen).to(torch.bfloat16).to(dev)
-        vc = torch.randn(B, NKV, P, S, HD, generator=gen).to(torch.bfloat16).to(dev)
+        vc = torch.randn(B, NKV, P, S, HD, generator=gen).to(
+            torch.float16 if v_f16 else torch.bfloat16).to(dev)
         out = torch.empty_like(q)
-        ctx = cp.Context(NQ, NKV, HD, P, S, C, 0.0, fast_p)
+        ctx = cp.Context(NQ, NKV, HD, P, S, C, 0.0, fast_p, v_f16)
         need, blocks = ctx.splitkv_workspace(cl, ch, 0)
         ws = torch.empty(max(need // 4, 64), dtype=torch.float32, device=dev)
 
@@ -528,7 +530,7 @@ def run_splitkv(fast_p=False, reps=20, seed=11):
         gbs = (kv_bytes + io_bytes) / (graph_ms * 1e-3) / 1e9
         print(json.dumps({
             "mode": "splitkv", "workload": name, "cache_lens": cl, "chunk_lens": ch,
-            "precision": "fast_p" if fast_p else "accurate P",
+            "precision": precision_label(fast_p, v_f16), "v_cache": "f16" if v_f16 else "bf16",
             "row_blocks": sum(-(-c // 128) for c in ch), "work_blocks_split": blocks,
             "fused_ms": round(fused_ms, 4), "split_ms": round(split_ms, 4),
             "split_graph_ms": round(graph_ms, 4),
@@ -563,9 +565,10 @@ def main():
     ap.add_argument("--impl", default="cpattn", choices=["cpattn", "reference"])
     ap.add_argument("--config", default="32k", choices=sorted(BY_NAME))
     ap.add_argument("--fast-p", action="store_true", help="P rounded once to bf16")
-    ap.add_argument("--v-cache", default="bf16", choices=["bf16", "f16"],
-                    help="V cache format: f16 makes cache tiles take P in fp16 (one P.V "
-                         "product at the accurate mode's precision)")
+    ap.add_argument("--v-cache", default="f16", choices=["bf16", "f16"],
+                    help="V cache format (default f16: cache tiles take P in fp16, one P.V "
+                         "product at the accurate mode's precision; bf16: the bf16 hi+lo P "
+                         "pair on every tile)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", default="fused", choices=["fused", "two_launch", "fused_write"],
                     help="fused_write: the KV write inside the prefill launch; "
@@ -580,13 +583,13 @@ def main():
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.splitkv:
-        run_splitkv(fast_p=args.fast_p)
+        run_splitkv(fast_p=args.fast_p, v_f16=args.v_cache == "f16")
         return
     if args.cumulative:
         mult = {"k": 1024, "m": 1024 * 1024}
         ns = [int(x[:-1]) * mult[x[-1].lower()] if x[-1].lower() in mult else int(x)
               for x in args.cumulative.split(",")]
-        run_cumulative(ns, fast_p=args.fast_p)
+        run_cumulative(ns, fast_p=args.fast_p, v_f16=args.v_cache == "f16")
         return
     if args.impl == "reference":
         run_reference(args, world, rank)
