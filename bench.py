@@ -239,9 +239,10 @@ def time_steps(st: DeviceState, steps: int, warmup: int, flush):
 def time_e2e(st: DeviceState, steps: int, warmup: int):
     """The step through the public API with inputs in pinned host memory: the
     host->device copy of Q, K_new, V_new, write_kv + prefill, and the
-    device->host copy of O, every step.  Copies run on their own stream into
-    double-buffered device tensors, so step i+1's upload and step i-1's
-    download overlap step i's kernels, as a serving loop would run them."""
+    device->host copy of O, every step.  Uploads, kernels and downloads run on
+    three streams into double-buffered device tensors, so step i+1's upload
+    and step i-1's download overlap step i's kernels, as a serving loop would
+    run them."""
     import torch
     w = st.w
     hq = st.inp.q.pin_memory()
@@ -251,27 +252,29 @@ def time_e2e(st: DeviceState, steps: int, warmup: int):
     dev = st.q.device
     bufs = [dict(q=torch.empty_like(st.q), k=torch.empty_like(st.k_new),
                  v=torch.empty_like(st.v_new), o=torch.empty_like(st.out)) for _ in range(2)]
-    # Two non-default streams: the legacy default stream would serialise them.
-    cs = torch.cuda.Stream(device=dev)  # copies
+    # Non-default streams: the legacy default stream would serialise them.
+    up = torch.cuda.Stream(device=dev)  # host -> device
     ks = torch.cuda.Stream(device=dev)  # kernels
+    dn = torch.cuda.Stream(device=dev)  # device -> host
     ev = lambda: torch.cuda.Event()
-    inputs_free = [ev() for _ in range(2)]      # kernels of the slot's last step done
-    output_free = [ev() for _ in range(2)]      # download of the slot's last output done
-    ks.wait_stream(torch.cuda.current_stream(device=dev))
-    for e in inputs_free + output_free:
+    kernels_done = [ev() for _ in range(2)]     # the slot's last kernels finished
+    output_free = [ev() for _ in range(2)]      # the slot's last output downloaded
+    for stream in (up, ks, dn):
+        stream.wait_stream(torch.cuda.current_stream(device=dev))
+    for e in kernels_done + output_free:
         e.record(ks)
 
     def one(i):
         s = i & 1
         b = bufs[s]
-        with torch.cuda.stream(cs):
-            cs.wait_event(inputs_free[s])
+        with torch.cuda.stream(up):
+            up.wait_event(kernels_done[s])
             b["q"].copy_(hq, non_blocking=True)
             b["k"].copy_(hk, non_blocking=True)
             b["v"].copy_(hv, non_blocking=True)
-            up = ev()
-            up.record(cs)
-        ks.wait_event(up)
+            uploaded = ev()
+            uploaded.record(up)
+        ks.wait_event(uploaded)
         ks.wait_event(output_free[s])
         if st.variant != "fused_write":
             st.ctx.write_kv(w.cache_lens, w.chunk_lens, b["k"], b["v"], st.k_cache, st.v_cache,
@@ -285,20 +288,21 @@ def time_e2e(st: DeviceState, steps: int, warmup: int):
         else:
             st.ctx.prefill(w.cache_lens, w.chunk_lens, b["q"], b["k"], b["v"], st.k_cache,
                            st.v_cache, b["o"], None, ks)
-        inputs_free[s].record(ks)
-        with torch.cuda.stream(cs):
-            cs.wait_event(inputs_free[s])
+        kernels_done[s].record(ks)
+        with torch.cuda.stream(dn):
+            dn.wait_event(kernels_done[s])
             ho[s].copy_(b["o"], non_blocking=True)
-            output_free[s].record(cs)
+            output_free[s].record(dn)
 
     for i in range(warmup):
         one(i)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(cs)
+    e0.record(up)
     for i in range(steps):
         one(i)
-    ks.wait_stream(cs)
+    ks.wait_stream(up)
+    ks.wait_stream(dn)
     e1.record(ks)
     torch.cuda.synchronize(dev)
     if st.ctx.sync_status() != 0:
@@ -651,7 +655,7 @@ def main():
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "note": "pinned host buffers; copies on a second stream overlap the previous/next step"},
+                "note": "pinned host buffers; uploads and downloads on their own streams overlap the previous/next step's kernels"},
         "gpu_launches": {"fused": 2, "two_launch": 4, "fused_write": 1}[args.variant] * args.steps,
         "clocks": clk.summary(),
     }
