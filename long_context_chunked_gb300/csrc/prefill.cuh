@@ -528,10 +528,6 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
     for (int v = 0; v < U.n_tiles; ++v) {
       const int va = U.v0 + v;  // virtual tile index within the unit's whole walk
       const uint32_t sb = tile_ctr & 1u;
-      ok = wait(bar(Ly::B_SFULL + sb), (tile_ctr >> 1) & 1u, kSiteSFull);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) *pair_fail = 1;  // decided at the vote below, together with the group
-      tc_fence_after();
       const uint32_t s_tmem = lane_tmem + HD + sb * kBKV + CW * h;
 
       // Region by value: one scalar picks the validity words of the tile.
@@ -564,6 +560,11 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
         all_valid &= wv;
       }
       const bool need_mask = __any_sync(0xFFFFFFFFu, all_valid != 0xFFFFFFFFu);
+      // The mask words need no S: they are ready before S is.
+      ok = wait(bar(Ly::B_SFULL + sb), (tile_ctr >> 1) & 1u, kSiteSFull);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) *pair_fail = 1;  // decided at the vote below, together with the group
+      tc_fence_after();
 
       // Pass 1: load this group's CW logits (all TMEM loads in flight
       // together), mask by value, and take their max.  The registers stay
