@@ -136,7 +136,8 @@ cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* 
  * may run before or after this call.
  *   q                   device bf16 [B*C, NQ, HD], token order
  *   k_new, v_new        device bf16 [B*C, NKV, HD]
- *   k_cache, v_cache    device bf16 [B, NKV, P, S, HD]
+ *   k_cache             device bf16 [B, NKV, P, S, HD]
+ *   v_cache             the same, bf16 or (v_cache_f16) fp16
  *   out                 device bf16 [B*C, NQ, HD]; pad rows are not written
  *   lse                 device fp32 [B*C, NQ] natural-log sum-exp of the
  *                       scaled logits, or NULL; pad rows not written
@@ -145,6 +146,9 @@ cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* 
  * query rows are 128/G tokens x the G q heads of one kv head, instead of
  * 128 tokens of one q head, so a decode step fills the tensor-core tile
  * instead of one row of it.
+ * Precision of P in P.V: with a bf16 V cache, P is carried as a bf16 hi + lo
+ * pair (fast_p: P rounded once to bf16); with an fp16 V cache, cache tiles
+ * take P in fp16 against the fp16 V and current-chunk tiles follow fast_p.
  * One kernel launch -- unless a split-KV workspace is registered
  * (cpattn_set_splitkv) and the batch's plan cuts some walks, in which case a
  * second, merge kernel follows on the same stream.
@@ -160,10 +164,11 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
 
 /*
  * cpattn_prefill and cpattn_write_kv of the same chunk in ONE launch (the
- * KV write fused into the prefill kernel).  Idle lanes of each CTA's load
- * warp copy the chunk's valid K/V rows into the striped caches while the
- * prefill runs.  The copy is the same bit copy as cpattn_write_kv: every
- * (token, kv head) once, pad rows and every other cache row untouched.  It
+ * KV write fused into the prefill kernel).  A dedicated writer warp of each
+ * CTA copies the chunk's valid K/V rows into the striped caches while the
+ * prefill runs.  The copy writes what cpattn_write_kv writes (bits, and V
+ * converted for an fp16 V cache): every (token, kv head) once, pad rows and
+ * every other cache row untouched.  It
  * cannot race the prefill: it writes only rows of tokens >= L_b, which the
  * prefill never reads as keys.  Cache tiles at a shard's edge may load those
  * rows as masked columns, and they hold finite values before and after.
