@@ -236,7 +236,7 @@ def time_steps(st: DeviceState, steps: int, warmup: int, flush):
     return step_ms, prefill_ms
 
 
-def time_e2e(st: DeviceState, steps: int, warmup: int):
+def time_e2e(st: DeviceState, steps: int, warmup: int, slots: int = 2):
     """The step through the public API with inputs in pinned host memory: the
     host->device copy of Q, K_new, V_new, write_kv + prefill, and the
     device->host copy of O, every step.  Uploads, kernels and downloads run on
@@ -248,24 +248,24 @@ def time_e2e(st: DeviceState, steps: int, warmup: int):
     hq = st.inp.q.pin_memory()
     hk = st.inp.k_new.pin_memory()
     hv = st.inp.v_new.pin_memory()
-    ho = [torch.empty_like(hq).pin_memory() for _ in range(2)]
+    ho = [torch.empty_like(hq).pin_memory() for _ in range(slots)]
     dev = st.q.device
     bufs = [dict(q=torch.empty_like(st.q), k=torch.empty_like(st.k_new),
-                 v=torch.empty_like(st.v_new), o=torch.empty_like(st.out)) for _ in range(2)]
+                 v=torch.empty_like(st.v_new), o=torch.empty_like(st.out)) for _ in range(slots)]
     # Non-default streams: the legacy default stream would serialise them.
     up = torch.cuda.Stream(device=dev)  # host -> device
     ks = torch.cuda.Stream(device=dev)  # kernels
     dn = torch.cuda.Stream(device=dev)  # device -> host
     ev = lambda: torch.cuda.Event()
-    kernels_done = [ev() for _ in range(2)]     # the slot's last kernels finished
-    output_free = [ev() for _ in range(2)]      # the slot's last output downloaded
+    kernels_done = [ev() for _ in range(slots)]  # the slot's last kernels finished
+    output_free = [ev() for _ in range(slots)]   # the slot's last output downloaded
     for stream in (up, ks, dn):
         stream.wait_stream(torch.cuda.current_stream(device=dev))
     for e in kernels_done + output_free:
         e.record(ks)
 
     def one(i):
-        s = i & 1
+        s = i % slots
         b = bufs[s]
         with torch.cuda.stream(up):
             up.wait_event(kernels_done[s])
