@@ -154,7 +154,8 @@ FULL = [CTX_8K, CTX_32K, CTX_128K, VARLEN]
 def test_full_size_sampled(w):
     """The benchmarked workloads at full size with the fp16 V cache, in the
     launch configuration the benchmark times: sampled rows against the oracle
-    (first/last rows of each sequence and q-block edges included)."""
+    (first/last rows of each sequence and q-block edges included), reading V
+    as stored and as the original bf16 values."""
     case = make_case(w, v_f16=True)
     dc = DeviceCase(case)
     ctx = cp.Context.for_workload(w, v_cache_f16=True)
@@ -164,6 +165,10 @@ def test_full_size_sampled(w):
     out = to_f64(dc.out.bits())
     got = np.stack([out[t, h] for t, h in samples])
     compare(got, ref, w.name)
+    # Also against the attention of the original bf16 V values (the fp16
+    # conversion is exact for them but below 2^-14).
+    ref_bf16, _ = make_case(w).oracle_rows(samples)
+    compare(got, ref_bf16, w.name + " vs bf16 V")
     lse = dc.lse.cpu().numpy()
     assert np.max(np.abs(np.array([lse[t, h] for t, h in samples]) - ref_lse)) < 2e-3
     v = dc.valid_rows()
