@@ -40,13 +40,15 @@ constexpr int kMaxPieceCandidates = 64;
 constexpr long long kPieceWriteBytesPerTile = 64 << 10;
 constexpr long long kMergeBytesPerTile = 10 << 20;
 
-// Cost model of a plan: the persistent grid hands units out cyclically in list
-// order -- executor e runs units e, e + E, e + 2E, ... -- and a unit costs its
-// tiles plus a fixed fill/drain overhead.  `lens` holds one entry per work
-// block, longest first (any per-unit extra cost already added); each block
-// has units_per_block units.  With the list sorted, executor 0 takes the
-// longest unit of every round and has the most rounds, so its load is the
-// makespan: O(rounds), no per-executor state.
+// Cost model of a plan: the persistent grid deals units out in rounds of E
+// in list order, and a unit costs its tiles plus a fixed fill/drain
+// overhead.  `lens` holds one entry per work block, longest first (any
+// per-unit extra cost already added); each block has units_per_block units.
+// The kernels deal each round in snake order (executor e takes slot e of
+// even rounds, slot E-1-e of odd ones); the model charges every round its
+// first, longest unit -- the load of executor 0 under a cyclic deal -- which
+// bounds every executor's snake load from above: O(rounds), no per-executor
+// state.
 inline long long cyclic_makespan(const std::vector<int>& lens, int units_per_block,
                                  int executors) {
   const long long total = static_cast<long long>(lens.size()) * units_per_block;

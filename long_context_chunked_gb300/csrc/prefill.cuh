@@ -180,6 +180,24 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
   return U;
 }
 
+// The r-th unit of this CTA.  Units are sorted longest first, and they are
+// dealt to the executors in boustrophedon order: executor e takes slot e of
+// even rounds and slot E-1-e of odd ones.  Dealt cyclically, the same
+// executor would take the longest unit of every round; the snake order cuts
+// the grid's makespan over the average from 8.4 % to 2.9 % on the 8k
+// workload (1.038 -> 1.022 on varlen).  An executor is a CTA, or a cluster
+// of `pair` CTAs that take adjacent units (two q heads of one kv head).
+// Every role of a CTA walks the same sequence; it ends at the first unit
+// index >= num_units (later rounds only hold larger indices).
+template <int PAIR>
+__device__ __forceinline__ int unit_of(int r) {
+  const int E = static_cast<int>(gridDim.x) / PAIR;
+  const int e = static_cast<int>(blockIdx.x) / PAIR;
+  const int rank = static_cast<int>(blockIdx.x) % PAIR;
+  const int slot = (r & 1) ? E - 1 - e : e;
+  return r * static_cast<int>(gridDim.x) + slot * PAIR + rank;
+}
+
 // Ring position shared by producer and consumer.
 struct RingPos {
   int slot = 0;
@@ -248,7 +266,7 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
     return true;
   };
 
-  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+  for (int ur = 0, u = unit_of<MC ? 2 : 1>(0); ok && u < p.num_units; u = unit_of<MC ? 2 : 1>(++ur)) {
     const Unit U = decode_unit(p, u);
     if (q_issued > 0 && !wait(bar(Ly::B_QEMPTY), (q_issued - 1) & 1u, kSiteQEmpty)) {
       ok = false;
@@ -318,10 +336,10 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
 // exactly once per launch.  These cache rows hold tokens >= L_b, which no
 // unit of this launch reads as keys.  16-byte vectors, consecutive lanes on
 // consecutive vectors of a row.
-template <int HD, bool VF16>
+template <int HD, bool VF16, int CL>
 __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane) {
   constexpr int VECS = HD * 2 / 16;  // 16-byte vectors per row
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+  for (int ur = 0, u = unit_of<CL>(0); u < p.num_units; u = unit_of<CL>(++ur)) {
     const Unit U = decode_unit(p, u);
     if (U.h % p.group != 0 || U.v0 != 0) continue;
     const int rows = min(p.packed ? p.tb : kBQ, U.c - U.q0);  // valid tokens of the block
@@ -423,7 +441,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
     return issue_pv_as(w, t, std::false_type{});
   };
 
-  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
+  for (int ur = 0, u = unit_of<MC ? 2 : 1>(0); ok && u < p.num_units; u = unit_of<MC ? 2 : 1>(++ur), ++units) {
     const Unit U = decode_unit(p, u);
     if (!wwait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
       ok = false;
@@ -486,7 +504,7 @@ __device__ __forceinline__ uint32_t causal_word(int lim, int q) {
 // PAIR2: the CTA is one of a pair whose leader issues 2-SM MMAs; S, P and O
 // of this CTA's 128 rows sit in its own TMEM exactly as in a single CTA, but
 // "P ready" goes to the leader's barrier, one arrival per warp.
-template <int HD, bool SPLIT, bool PAIR2, bool VF16>
+template <int HD, bool SPLIT, bool PAIR2, bool VF16, int CL>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                              const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -512,7 +530,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
   bool drop_one = (p.debug_flags & kDebugDropArrive) && blockIdx.x == 0 && threadIdx.x == 0;
   constexpr int OCOLS = HD / NG;                        // O columns of this group
 
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+  for (int ur = 0, u = unit_of<CL>(0); u < p.num_units; u = unit_of<CL>(++ur)) {
     const Unit U = decode_unit(p, u);
     // This row's token (within the chunk) and q head.
     const int tok = U.q0 + (p.packed ? r / p.group : r);
@@ -826,11 +844,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
 
   if (warp < kProducerWarp) {
-    softmax_role<HD, SPLIT, false, VF16>(p, sbase, tmem, wait);
+    softmax_role<HD, SPLIT, false, VF16, MC ? 2 : 1>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role<HD, MC>(p, sbase, wait);
   } else if (warp == kWriterWarp) {
-    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16>(p, lane);
+    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, MC ? 2 : 1>(p, lane);
   } else {
     mma_role<HD, SPLIT, MC, VF16>(p, sbase, tmem, wait);
   }

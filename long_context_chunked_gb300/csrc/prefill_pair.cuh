@@ -81,7 +81,7 @@ __device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint
     return true;
   };
 
-  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+  for (int ur = 0, u = unit_of<2>(0); ok && u < p.num_units; u = unit_of<2>(++ur)) {
     const Unit U = decode_unit(p, u);
     if (q_issued > 0 && !wait(bar(Ly::B_QEMPTY), (q_issued - 1) & 1u, kSiteQEmpty)) {
       ok = false;
@@ -230,7 +230,7 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
     return issue_pv_as(w, t, std::false_type{});
   };
 
-  for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++units) {
+  for (int ur = 0, u = unit_of<2>(0); ok && u < p.num_units; u = unit_of<2>(++ur), ++units) {
     const Unit U = decode_unit(p, u);
     if (!wwait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
       ok = false;
@@ -278,9 +278,10 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
 }
 
 // ------------------------------------------------------------------ kernel
-// Launched with clusters of two CTAs; CTA 2k + r runs units u = 2k + r +
-// m * gridDim.x, so the pair always holds q heads 2i and 2i + 1 of the same
-// row block (the host launches it only when the group size is even).
+// Launched with clusters of two CTAs; CTA 2k + r runs units 2s + r of each
+// round of gridDim.x units (s = k in even rounds, E - 1 - k in odd ones:
+// unit_of), so the pair always holds q heads 2i and 2i + 1 of the same row
+// block (the host launches it only when the group size is even).
 template <int HD, bool SPLIT, bool VF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel_pair2(const __grid_constant__ PrefillParams p) {
@@ -331,11 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
 
   if (warp < kProducerWarp) {
-    softmax_role<HD, SPLIT, true, VF16>(p, sbase, tmem, wait);
+    softmax_role<HD, SPLIT, true, VF16, 2>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
   } else if (warp == kWriterWarp) {
-    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16>(p, lane);
+    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 2>(p, lane);
   } else if (warp == kMmaWarp && rank == 0) {
     mma_role_pair2<HD, SPLIT, VF16>(p, sbase, tmem, wait);
   }
