@@ -47,7 +47,8 @@ def load_peaks():
 # Device sources each profiled kernel is built from, and the work plan that
 # shapes its launch; a DRAM record holds while these are unchanged.
 KERNEL_SOURCES = {
-    "prefill": ("prefill.cuh", "prefill_pair.cuh", "walk.cuh", "ptx.cuh", "plan.h"),
+    "prefill": ("prefill.cuh", "prefill_pair.cuh", "prefill_pingpong.cuh", "walk.cuh", "ptx.cuh",
+                "plan.h"),
     "write_kv": ("write_kv.cuh",),
 }
 
@@ -62,10 +63,12 @@ def csrc_hash(kernel: str) -> str:
 
 
 def prefill_kernel_name(w) -> str:
-    """The prefill kernel the library launches for this workload: paired CTAs
+    """The prefill kernel the library launches for this workload: paired heads
     (CPATTN_PAIRING, default 2-SM MMA) when the group size is even."""
     mode = os.environ.get("CPATTN_PAIRING", "mma2") if w.group % 2 == 0 else "none"
-    if mode == "mma2":
+    if mode == "pingpong" and w.head_dim == 128:
+        return "prefill_kernel_pingpong<128>"
+    if mode in ("mma2", "pingpong"):
         return "prefill_kernel_pair2<%d>" % w.head_dim
     if mode == "multicast":
         return "prefill_kernel<%d> (multicast pairs)" % w.head_dim

@@ -90,11 +90,13 @@ typedef struct cpattn_ctx cpattn_ctx; /* opaque */
  * current device (skipped, without error, when no device is present; launches
  * then fail with CPATTN_E_CUDA).
  * The environment variable CPATTN_PAIRING, read here, picks how prefill
- * pairs the CTAs of adjacent q heads of one kv head when NQ/NKV is even:
- * "mma2" (default: the pair runs 2-SM tensor-core MMAs and each SM stages
- * half of every K/V tile), "multicast" (each CTA runs its own MMAs, the pair
- * shares K/V loads), "none" (one CTA per unit).  Results meet the same
- * accuracy in every mode; the bits may differ between modes.
+ * pairs adjacent q heads of one kv head when NQ/NKV is even: "mma2"
+ * (default: a CTA pair runs 2-SM tensor-core MMAs and each SM stages half of
+ * every K/V tile), "multicast" (each CTA of a pair runs its own MMAs, the
+ * pair shares K/V loads), "pingpong" (HD = 128: one CTA holds both heads'
+ * query tiles and alternates their products with their softmaxes; "mma2" at
+ * HD = 256), "none" (one CTA per unit).  Results meet the same accuracy in
+ * every mode; the bits may differ between modes.
  * CPATTN_GQA_PACKING ("auto", the default, or "off"), also read here,
  * controls the packed form of short-chunk launches described at
  * cpattn_prefill.

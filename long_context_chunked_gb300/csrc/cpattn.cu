@@ -17,6 +17,7 @@
 #include "cpattn.h"
 #include "prefill.cuh"
 #include "prefill_pair.cuh"
+#include "prefill_pingpong.cuh"
 #include "walk.cuh"
 #include "write_kv.cuh"
 #include "merge.cuh"
@@ -27,9 +28,10 @@ struct cpattn_ctx {
   int device = -1;
   int num_sms = 0;
   int* d_status = nullptr;           // device status word (timeouts)
-  int grid_cap[2][2][3][2] = {};  // [HD == 256][split P][pairing mode][fp16 V cache]: 0 until set up
-  // CTA pairing for even group sizes (CPATTN_PAIRING = mma2 | multicast | none):
-  // 2 = 2-SM MMA pairs, 1 = pairs sharing K/V loads by multicast, 0 = off.
+  int grid_cap[2][2][4][2] = {};  // [HD == 256][split P][pairing mode][fp16 V cache]: 0 until set up
+  // Head pairing for even group sizes (CPATTN_PAIRING = mma2 | multicast |
+  // pingpong | none): 2 = 2-SM MMA pairs, 1 = CTA pairs sharing K/V loads by
+  // multicast, 3 = two query tiles per CTA (HD = 128; 2 at HD = 256), 0 = off.
   int pair_mode = 2;
   // Split-KV: a caller-owned device workspace and the policy (kSplitOff,
   // kSplitAuto, or a forced piece length in tiles); off until registered.
@@ -128,15 +130,21 @@ cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* wha
 
 template <int HD, bool SPLIT, int MODE, bool VF16>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
-  using Ly = cpattn::Layout<HD>;
-  constexpr bool MC = MODE != 0;  // launched as clusters of two CTAs
-  void (*kernel)(cpattn::PrefillParams) = MODE == 2
-                                              ? cpattn::prefill_kernel_pair2<HD, SPLIT, VF16>
-                                              : cpattn::prefill_kernel<HD, SPLIT, MODE == 1, VF16>;
+  static_assert(MODE != 3 || HD == 128, "two query tiles per CTA only at HD = 128");
+  constexpr bool MC = MODE == 1 || MODE == 2;  // launched as clusters of two CTAs
+  constexpr int SMEM_BYTES =
+      MODE == 3 ? cpattn::PingPongLayout::SMEM_BYTES : cpattn::Layout<HD>::SMEM_BYTES;
+  void (*kernel)(cpattn::PrefillParams);
+  if constexpr (MODE == 3)
+    kernel = cpattn::prefill_kernel_pingpong<SPLIT, VF16>;
+  else if constexpr (MODE == 2)
+    kernel = cpattn::prefill_kernel_pair2<HD, SPLIT, VF16>;
+  else
+    kernel = cpattn::prefill_kernel<HD, SPLIT, MODE == 1, VF16>;
   int& grid_cap = ctx->grid_cap[HD == 256][SPLIT][MODE][VF16];
   if (grid_cap == 0) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Ly::SMEM_BYTES);
+                                         SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(prefill)");
     grid_cap = ctx->num_sms;
     if (MC) {
@@ -144,7 +152,7 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
       cudaLaunchConfig_t q = {};
       q.gridDim = dim3(2 * ctx->num_sms, 1, 1);
       q.blockDim = dim3(cpattn::kThreads, 1, 1);
-      q.dynamicSmemBytes = Ly::SMEM_BYTES;
+      q.dynamicSmemBytes = SMEM_BYTES;
       cudaLaunchAttribute a[1];
       a[0].id = cudaLaunchAttributeClusterDimension;
       a[0].val.clusterDim.x = 2;
@@ -161,12 +169,13 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
       grid_cap = std::min(2 * clusters, ctx->num_sms & ~1);
     }
   }
-  int grid = std::min(prm->num_units, grid_cap);
+  // A CTA of MODE 3 takes two units (a head pair) per round.
+  int grid = std::min(MODE == 3 ? prm->num_units / 2 : prm->num_units, grid_cap);
   if (MC) grid &= ~1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(cpattn::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Ly::SMEM_BYTES;
+  cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -180,9 +189,19 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
   return after_launch(ctx, stream, "prefill launch");
 }
 
+// The pairing mode a launch runs in: none for packed units (they hold a
+// whole kv group already) or odd group sizes; two query tiles per CTA only
+// at HD = 128 (the 2-SM pairs at HD = 256, whose O fills half of TMEM).
+int launch_pair_mode(const cpattn_ctx* ctx, bool packed) {
+  const cpattn_config& c = ctx->cfg;
+  if (packed || (c.num_q_heads / c.num_kv_heads) % 2 != 0) return 0;
+  if (ctx->pair_mode == 3 && c.head_dim != 128) return 2;
+  return ctx->pair_mode;
+}
+
 // The plan's executors and units per work block: SM pairs and q-head pairs
-// when the prefill runs as CTA pairs, else SMs and q heads (148 SMs when no
-// device is present, for host-side planning).
+// for CTA pairs, SMs and q-head pairs for two query tiles per CTA, else SMs
+// and q heads (148 SMs when no device is present, for host-side planning).
 void plan_shape(const cpattn_ctx* ctx, bool packed, int* executors, int* units_per_block) {
   const int sms = ctx->num_sms > 0 ? ctx->num_sms : 148;
   if (packed) {  // one unit per kv head, unpaired
@@ -190,9 +209,9 @@ void plan_shape(const cpattn_ctx* ctx, bool packed, int* executors, int* units_p
     *units_per_block = ctx->cfg.num_kv_heads;
     return;
   }
-  const bool paired = ctx->pair_mode != 0 && (ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads) % 2 == 0;
-  *executors = paired ? sms / 2 : sms;
-  *units_per_block = paired ? ctx->cfg.num_q_heads / 2 : ctx->cfg.num_q_heads;
+  const int mode = launch_pair_mode(ctx, packed);
+  *executors = (mode == 1 || mode == 2) ? sms / 2 : sms;
+  *units_per_block = mode != 0 ? ctx->cfg.num_q_heads / 2 : ctx->cfg.num_q_heads;
 }
 
 // GQA packing: a unit's 128 rows become (token, q head of one kv group) when
@@ -213,6 +232,10 @@ int pack_block_tokens(const cpattn_ctx* ctx, int32_t num_seqs, const int32_t* ch
 template <int HD, bool VF16>
 cpattn_status dispatch_prefill_hd(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st,
                                   bool split, int mode) {
+  if constexpr (HD == 128) {
+    if (mode == 3) return split ? launch_prefill<HD, true, 3, VF16>(ctx, prm, st)
+                                : launch_prefill<HD, false, 3, VF16>(ctx, prm, st);
+  }
   if (mode == 2) return split ? launch_prefill<HD, true, 2, VF16>(ctx, prm, st)
                               : launch_prefill<HD, false, 2, VF16>(ctx, prm, st);
   if (mode == 1) return split ? launch_prefill<HD, true, 1, VF16>(ctx, prm, st)
@@ -226,9 +249,8 @@ cpattn_status dispatch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cuda
   const int HD = ctx->cfg.head_dim;
   const bool split = ctx->cfg.fast_p == 0;
   const bool vf16 = ctx->cfg.v_cache_f16 != 0;
-  // Pair CTAs on adjacent q heads of one kv head when the group size allows
-  // (packed units hold a whole group already: one CTA each).
-  const int mode = (!packed && prm->group % 2 == 0) ? ctx->pair_mode : 0;
+  // Pair adjacent q heads of one kv head when the group size allows.
+  const int mode = launch_pair_mode(ctx, packed);
   if (HD == 256)
     return vf16 ? dispatch_prefill_hd<256, true>(ctx, prm, st, split, mode)
                 : dispatch_prefill_hd<256, false>(ctx, prm, st, split, mode);
@@ -421,6 +443,7 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
     if (std::strcmp(pairing, "none") == 0) ctx->pair_mode = 0;
     else if (std::strcmp(pairing, "multicast") == 0) ctx->pair_mode = 1;
     else if (std::strcmp(pairing, "mma2") == 0) ctx->pair_mode = 2;
+    else if (std::strcmp(pairing, "pingpong") == 0) ctx->pair_mode = 3;
     else {
       delete ctx;
       return CPATTN_E_INVALID;

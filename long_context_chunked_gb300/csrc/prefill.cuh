@@ -335,11 +335,11 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
 // -- the strided write of write_kv.cuh, so every (token, kv head) is written
 // exactly once per launch.  These cache rows hold tokens >= L_b, which no
 // unit of this launch reads as keys.  16-byte vectors, consecutive lanes on
-// consecutive vectors of a row.
-template <int HD, bool VF16, int CL>
-__device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane) {
+// consecutive vectors of a row.  unit_at(i): this CTA's i-th unit.
+template <int HD, bool VF16, class UnitAt>
+__device__ __forceinline__ void kv_write_units(const PrefillParams& p, int lane, UnitAt unit_at) {
   constexpr int VECS = HD * 2 / 16;  // 16-byte vectors per row
-  for (int ur = 0, u = unit_of<CL>(0); u < p.num_units; u = unit_of<CL>(++ur)) {
+  for (int ur = 0, u = unit_at(0); u < p.num_units; u = unit_at(++ur)) {
     const Unit U = decode_unit(p, u);
     if (U.h % p.group != 0 || U.v0 != 0) continue;
     const int rows = min(p.packed ? p.tb : kBQ, U.c - U.q0);  // valid tokens of the block
@@ -360,6 +360,11 @@ __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane)
       reinterpret_cast<uint4*>(p.v_cache_w + dst)[x] = vv;
     }
   }
+}
+
+template <int HD, bool VF16, int CL>
+__device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane) {
+  kv_write_units<HD, VF16>(p, lane, [](int i) { return unit_of<CL>(i); });
 }
 
 // ------------------------------------------------------------- MMA issuer
@@ -493,6 +498,85 @@ namespace cpattn {
 __device__ __forceinline__ uint32_t causal_word(int lim, int q) {
   const int n = lim - 32 * q;
   return n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+// p = 2^(x*sl2 - m) over one chunk of 32 logits of a row (x: fp32 bits),
+// accumulated into the row sum (lsa: even pairs, lsb: odd pairs) and stored
+// as P over the chunk's 32 TMEM columns at taddr: P_hi = bf16(p) in the
+// first 16 and, SPLIT, P_lo = bf16(p - P_hi) in the next 16; F16 (a tile of
+// an fp16 V cache): fp16(p) in the first 16 (one P.V product).
+template <bool SPLIT, bool F16>
+__device__ __forceinline__ void exp_pack_store(const uint32_t (&x)[32], uint32_t taddr,
+                                               float2 sl2x2, float2 negm2, float2& lsa,
+                                               float2& lsb) {
+  const float2 minus1 = make_float2(-1.f, -1.f);
+  uint32_t hi[16], lo[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 y = __ffma2_rn(
+        make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), sl2x2, negm2);
+    const float2 pab = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+    if (i & 1) lsb = __fadd2_rn(lsb, pab); else lsa = __fadd2_rn(lsa, pab);
+    if (F16) {
+      hi[i] = pack_f16x2(pab.x, pab.y);
+    } else {
+      hi[i] = pack_bf16x2(pab.x, pab.y);
+      if (SPLIT) {
+        const float2 hf = make_float2(__uint_as_float(hi[i] << 16),
+                                      __uint_as_float(hi[i] & 0xFFFF0000u));
+        const float2 res = __ffma2_rn(hf, minus1, pab);
+        lo[i] = pack_bf16x2(res.x, res.y);
+      }
+    }
+  }
+  tmem_st16(taddr, hi);
+  if (SPLIT && !F16) tmem_st16(taddr + 16, lo);
+}
+
+// One output row of a unit from its O columns [ocol0, ocol0 + OCOLS) in
+// TMEM (o_tmem: this warp's lanes, column ocol0): a split-KV piece writes
+// fp32 O / l and its LSE to its partial rows; a whole unit writes the output
+// row (bf16, or fp32 when out_f32).  Rows past the chunk are not written.
+// with_lse: this thread also writes the row's LSE, (m + log2 l) ln 2.
+template <int HD, int OCOLS>
+__device__ __forceinline__ void store_row(const PrefillParams& p, const Unit& U, int row, int head,
+                                          int ocol0, uint32_t o_tmem, float m, float l_row,
+                                          bool with_lse) {
+  const bool valid = row < U.c;
+  const float inv_l = 1.f / l_row;
+  const bool partial = U.part >= 0;
+  const long long tok_g = static_cast<long long>(U.b) * p.C + row;  // token-order row
+  const long long orow_i =
+      (partial ? static_cast<long long>(U.part + (row - U.q0)) : tok_g) * p.nq + head;
+  const bool f32 = partial || p.out_f32 != 0;
+  float* lse_out = partial ? p.ws_lse : p.lse;
+  uint4* orow = reinterpret_cast<uint4*>(p.out + orow_i * HD + ocol0);
+  float4* orow32 = reinterpret_cast<float4*>((partial ? p.ws_o : reinterpret_cast<float*>(p.out)) +
+                                             orow_i * HD + ocol0);
+#pragma unroll 1
+  for (int ch = 0; ch < OCOLS / 32; ++ch) {
+    uint32_t o[32];
+    tmem_ld32_wait(o_tmem + 32 * ch, o);
+    if (valid && f32) {
+#pragma unroll
+      for (int v4 = 0; v4 < 8; ++v4)
+        orow32[ch * 8 + v4] = make_float4(
+            __uint_as_float(o[4 * v4]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
+            __uint_as_float(o[4 * v4 + 2]) * inv_l, __uint_as_float(o[4 * v4 + 3]) * inv_l);
+    } else if (valid) {
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) {
+        uint4 pk;
+        pk.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
+        pk.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
+        pk.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
+        pk.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
+        orow[ch * 4 + v4] = pk;
+      }
+    }
+  }
+  if (with_lse && valid && lse_out != nullptr)
+    lse_out[orow_i] = (m + __log2f(l_row)) * 0.69314718055994531f;
 }
 
 // ------------------------------------------------------- softmax + epilogue
@@ -641,47 +725,21 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       const float2 sl2x2 = make_float2(sl2, sl2);
       const float2 negm2 = make_float2(neg_m, neg_m);
-      const float2 minus1 = make_float2(-1.f, -1.f);
       float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
       {
-        // F16: a tile of an fp16 V cache takes P in fp16 (11-bit significand,
-        // one P.V product); otherwise P_hi in bf16 and, accurate mode, P_lo.
-        auto chunk_exp = [&](const uint32_t (&x)[32], int q, auto f16tag) {
-          constexpr bool F16 = decltype(f16tag)::value;
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 y = __ffma2_rn(
-                make_float2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), sl2x2,
-                negm2);
-            const float2 pab = make_float2(ex2_approx(y.x), ex2_approx(y.y));
-            if (i & 1) lsb = __fadd2_rn(lsb, pab); else lsa = __fadd2_rn(lsa, pab);
-            if (F16) {
-              hi[i] = pack_f16x2(pab.x, pab.y);
-            } else {
-              hi[i] = pack_bf16x2(pab.x, pab.y);
-              if (SPLIT) {
-                const float2 hf = make_float2(__uint_as_float(hi[i] << 16),
-                                              __uint_as_float(hi[i] & 0xFFFF0000u));
-                const float2 res = __ffma2_rn(hf, minus1, pab);
-                lo[i] = pack_bf16x2(res.x, res.y);
-              }
-            }
-          }
-          tmem_st16(s_tmem + 32 * q, hi);
-          if (SPLIT && !F16) tmem_st16(s_tmem + 32 * q + 16, lo);
-        };
         bool f16_done = false;
         if constexpr (VF16) {
           if (in_cache) {
 #pragma unroll
-            for (int c = 0; c < CH; ++c) chunk_exp(rr[c], c, std::true_type{});
+            for (int c = 0; c < CH; ++c)
+              exp_pack_store<SPLIT, true>(rr[c], s_tmem + 32 * c, sl2x2, negm2, lsa, lsb);
             f16_done = true;
           }
         }
         if (!f16_done) {
 #pragma unroll
-          for (int c = 0; c < CH; ++c) chunk_exp(rr[c], c, std::false_type{});
+          for (int c = 0; c < CH; ++c)
+            exp_pack_store<SPLIT, false>(rr[c], s_tmem + 32 * c, sl2x2, negm2, lsa, lsb);
         }
       }
       l = l * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
@@ -752,44 +810,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       continue;
     }
     tc_fence_after();
-    const int row = tok;
-    const bool valid = row < U.c;
-    const float inv_l = 1.f / l_row;
-    // A split-KV piece writes fp32 O / l and its LSE to its partial rows; a
-    // whole unit writes the output row (bf16, or fp32 when out_f32).
-    const bool partial = U.part >= 0;
-    const long long tok_g = static_cast<long long>(U.b) * p.C + row;  // token-order row
-    const long long orow_i =
-        (partial ? static_cast<long long>(U.part + (row - U.q0)) : tok_g) * p.nq + head;
-    const bool f32 = partial || p.out_f32 != 0;
-    float* lse_out = partial ? p.ws_lse : p.lse;
-    uint4* orow = reinterpret_cast<uint4*>(p.out + orow_i * HD + h * OCOLS);
-    float4* orow32 = reinterpret_cast<float4*>((partial ? p.ws_o : reinterpret_cast<float*>(p.out)) +
-                                               orow_i * HD + h * OCOLS);
-#pragma unroll 1
-    for (int ch = 0; ch < OCOLS / 32; ++ch) {
-      uint32_t o[32];
-      tmem_ld32_wait(lane_tmem + h * OCOLS + 32 * ch, o);
-      if (valid && f32) {
-#pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4)
-          orow32[ch * 8 + v4] = make_float4(
-              __uint_as_float(o[4 * v4]) * inv_l, __uint_as_float(o[4 * v4 + 1]) * inv_l,
-              __uint_as_float(o[4 * v4 + 2]) * inv_l, __uint_as_float(o[4 * v4 + 3]) * inv_l);
-      } else if (valid) {
-#pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          uint4 pk;
-          pk.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv_l, __uint_as_float(o[8 * v4 + 1]) * inv_l);
-          pk.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
-          pk.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
-          pk.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
-          orow[ch * 4 + v4] = pk;
-        }
-      }
-    }
-    if (h == 0 && valid && lse_out != nullptr)
-      lse_out[orow_i] = (m + __log2f(l_row)) * 0.69314718055994531f;
+    store_row<HD, OCOLS>(p, U, tok, head, h * OCOLS, lane_tmem + h * OCOLS, m, l_row, h == 0);
     tc_fence_before();
   }
 }

@@ -66,6 +66,7 @@ def test_create_rejects(lib, cfg, status):
 
 
 @pytest.mark.parametrize("value,ok", [("mma2", True), ("multicast", True), ("none", True),
+                                      ("pingpong", True),
                                       ("both", False), ("", False)])
 def test_pairing_mode_from_environment(lib, monkeypatch, value, ok):
     """CPATTN_PAIRING is read at create; an unknown value is rejected there

@@ -1,10 +1,12 @@
-"""The three CTA pairing modes of the fused prefill against the fp64 oracle.
+"""The head pairing modes of the fused prefill against the fp64 oracle.
 
-With an even group size the library pairs the CTAs of adjacent q heads of
-one kv head.  CPATTN_PAIRING (read when a context is created) picks how:
-'mma2' -- the leader CTA issues 2-SM MMAs (M = 256) and each CTA stages half
+With an even group size the library pairs adjacent q heads of one kv head.
+CPATTN_PAIRING (read when a context is created) picks how: 'mma2' -- the
+leader CTA of a CTA pair issues 2-SM MMAs (M = 256) and each CTA stages half
 of every K/V tile; 'multicast' -- each CTA issues its own MMAs and the pair
-shares K/V loads by multicast; 'none' -- one CTA per unit.  Every mode must
+shares K/V loads by multicast; 'pingpong' -- one CTA holds both heads' query
+tiles and alternates their products (HD = 128; 'mma2' at HD = 256);
+'none' -- one CTA per unit.  Every mode must
 meet the same bar on cases with several tiles, ragged chunks and an empty
 cache, in both P precisions."""
 import numpy as np
@@ -17,7 +19,7 @@ from workloads import small
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["mma2", "multicast", "none"]
+MODES = ["mma2", "multicast", "none", "pingpong"]
 CASES = [
     small("pairA", (0, 1000, 129), (300, 130, 256), 320, nq=8, nkv=2, hd=128, shards=4,
           shard_capacity=300, seed=41),

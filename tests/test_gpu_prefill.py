@@ -145,13 +145,16 @@ def test_repeatable_and_write_order_independent():
     assert np.array_equal(first, dc.out.bits())
 
 
-@pytest.mark.parametrize("hd,nq,nkv", [(128, 4, 2), (256, 8, 2), (128, 3, 3)])
-def test_rescale_on_every_tile(hd, nq, nkv):
+@pytest.mark.parametrize("hd,nq,nkv,mode", [(128, 4, 2, "mma2"), (256, 8, 2, "mma2"),
+                                             (128, 3, 3, "mma2"), (128, 4, 2, "pingpong")])
+def test_rescale_on_every_tile(hd, nq, nkv, mode, monkeypatch):
     """Keys constant along each row, stepping up by 0.5 per tile in walk
     order (cache flat rows, then the chunk's tiles), queries all ones: every
     tile's row max exceeds the running max by sqrt(HD) * 0.5 * log2(e) > 8, so
     the lazy rescale of O -- and its wait for the previous tile's P.V --
-    runs on every tile of every unit, in the paired and unpaired kernels."""
+    runs on every tile of every unit, in the paired, unpaired and two-tile
+    kernels."""
+    monkeypatch.setenv("CPATTN_PAIRING", mode)
     w = small(f"resc{hd}", (1500, 300), (300, 200), 320, nq=nq, nkv=nkv, hd=hd, shards=3,
               shard_capacity=700, seed=41 + hd)
     case = make_case(w)

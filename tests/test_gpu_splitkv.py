@@ -77,7 +77,7 @@ def test_forced_split_parity(w, t):
     _run(w, t)
 
 
-@pytest.mark.parametrize("mode", ["mma2", "none"])
+@pytest.mark.parametrize("mode", ["mma2", "none", "pingpong"])
 def test_forced_split_parity_pairing_modes(mode, monkeypatch):
     monkeypatch.setenv("CPATTN_PAIRING", mode)
     _run(CASES[0], 3)

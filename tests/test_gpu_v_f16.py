@@ -58,7 +58,7 @@ def test_parity(w, fast_p):
     _check(w, dc, case, fast_p)
 
 
-@pytest.mark.parametrize("mode", ["mma2", "multicast", "none"])
+@pytest.mark.parametrize("mode", ["mma2", "multicast", "none", "pingpong"])
 def test_pairing_modes(mode, monkeypatch):
     monkeypatch.setenv("CPATTN_PAIRING", mode)
     w = CASES[0]
