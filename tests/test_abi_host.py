@@ -226,3 +226,19 @@ def test_splitkv_workspace_too_small_is_refused_before_launch(lib):
     A = 256
     st = ctx.prefill_raw(cl, ch, A, A, A, A, A, A, None, stream=0)
     assert st == cp.E_INVALID and "split-KV workspace" in ctx.last_error()
+
+
+def test_pingpong_plans_per_sm(lib, monkeypatch):
+    """Two query tiles per CTA: every SM is an executor of head pairs, so a
+    short chunk against a long cache is cut into more pieces than for CTA
+    pairs (one executor per two SMs); at HD = 256 the mode runs as 2-SM
+    pairs and plans exactly like them."""
+    plans = {}
+    for mode in ("mma2", "pingpong"):
+        monkeypatch.setenv("CPATTN_PAIRING", mode)
+        for hd in (128, 256):
+            ctx = cp.Context(8, 2, hd, 8, 8000, 128)
+            plans[mode, hd] = ctx.splitkv_workspace([60000], [100], 0)
+            ctx.close()
+    assert plans["pingpong", 256] == plans["mma2", 256]
+    assert plans["pingpong", 128][1] > plans["mma2", 128][1] > 1
