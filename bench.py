@@ -212,7 +212,8 @@ class DeviceState:
 
 def time_steps(st: DeviceState, steps: int, warmup: int, flush):
     """Per-step device times (ms) of write_kv + prefill, and of prefill alone,
-    with an L2 flush between steps (outside the timed events)."""
+    with an L2 flush between steps (outside the timed events); flush=None
+    times them back to back with L2 left warm."""
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -224,7 +225,8 @@ def time_steps(st: DeviceState, steps: int, warmup: int, flush):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for e0, e1, e2 in ev:
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         e0.record(stream)
         st.write_kv()
         e1.record(stream)
@@ -625,6 +627,8 @@ def main():
     if world > 1:
         dist.barrier()
     e2e_ms, h2d, d2h = time_e2e(st, max(4, args.steps // 2), args.warmup)
+    # Context beside the flushed number: the same step with L2 left warm.
+    _, hot_prefill_ms = time_steps(st, min(args.steps, 20), 3, None)
 
     flops = w.attention_flops()
     kname = prefill_kernel_name(w)
@@ -647,6 +651,7 @@ def main():
                    "l2": "flushed between steps (512 MiB write)",
                    "parallelism": f"replicas x{world}", "variant": args.variant},
         "prefill_ms": round(pf, 4), "write_kv_ms": round(kv_ms, 4),
+        "prefill_ms_hot_l2": round(statistics.mean(hot_prefill_ms), 4),
         "write_kv_gbs": round(w.kv_write_bytes() / (kv_ms * 1e-3) / 1e9, 1) if kv_ms > 0 else None,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
