@@ -1,6 +1,8 @@
 """Plant plausible mistakes in the oracle (on the CPU) and check that the pins
 catch every one of them -- evidence that the pins constrain the oracle rather
-than restate it."""
+than restate it.  Covered: the attention arithmetic, the striped layout and
+write, the LSE merge, the working precision, and the bf16 -> fp16 conversion
+of the fp16 V cache."""
 import numpy as np
 import pytest
 
@@ -60,6 +62,36 @@ def _merge_swapped(o1, lse1, o2, lse2):
 
 
 _orig_as_f64 = oatt.as_f64
+_orig_f16 = ostr.bf16_to_f16_bits
+
+
+def _f16_toward_zero(u16):
+    """bf16 -> binary16 rounded toward zero instead of to nearest even."""
+    f32 = (np.asarray(u16).astype(np.uint32) << 16).view(np.float32)
+    with np.errstate(over="ignore"):
+        h = f32.astype(np.float16)
+    hb = h.view(np.uint16).copy()
+    up = np.abs(h.astype(np.float32)) > np.abs(f32)  # rounded away from zero
+    hb[up] -= 1  # one step smaller in magnitude, same sign
+    return hb
+
+
+def _f16_flush_subnormals(u16):
+    h = _orig_f16(u16).copy()
+    h[(h & 0x7C00) == 0] &= 0x8000
+    return h
+
+
+def _f16_saturating(u16):
+    h = _orig_f16(u16).copy()
+    inf = (h & 0x7FFF) == 0x7C00
+    h[inf] = (h[inf] & 0x8000) | 0x7BFF
+    return h
+
+
+def _write_v_unconverted(k_cache, v_cache, k_new, v_new, cache_lens, chunk_lens, chunk,
+                         v_f16=False):
+    return _orig_write(k_cache, v_cache, k_new, v_new, cache_lens, chunk_lens, chunk)
 
 MUTANTS = {
     "gqa map h mod G": (oatt, "kv_head_of", lambda h, g: h % g),
@@ -74,6 +106,10 @@ MUTANTS = {
     "write lands one token late": (ostr, "write_kv_ref", _write_off_by_one),
     "merge weights swapped": (oatt, "lse_merge", _merge_swapped),
     "fp32 instead of fp64": (oatt, "as_f64", lambda x: _orig_as_f64(x).astype(np.float32).astype(np.float64)),
+    "fp16 V rounded toward zero": (ostr, "bf16_to_f16_bits", _f16_toward_zero),
+    "fp16 V subnormals flushed": (ostr, "bf16_to_f16_bits", _f16_flush_subnormals),
+    "fp16 V overflow saturates": (ostr, "bf16_to_f16_bits", _f16_saturating),
+    "fp16 V cache written unconverted": (ostr, "write_kv_ref", _write_v_unconverted),
 }
 
 
