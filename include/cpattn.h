@@ -65,17 +65,41 @@ typedef struct {
                               about 2.2e-3 instead of 1.7e-3 on N(0,1) inputs) */
   int32_t v_cache_f16;     /* 0 (default): the V cache holds bf16, as k_cache;
                               1: the V cache holds fp16.  cpattn_write_kv then
-                              converts each bf16 value of v_new to fp16
-                              (round to nearest even: exact for normal values
-                              within fp16's range, |v| <= 65504); a value it
-                              cannot represent finitely is reported by the next
-                              cpattn_sync_status as CPATTN_E_RANGE.  Prefill
-                              then takes P in fp16 for cache tiles: one P.V
-                              product (11-bit P, relative RMS error about 1.7e-3
-                              on N(0,1) inputs, as the bf16 hi + lo pair) at the
-                              cost of fast_p.  Current-chunk tiles still read
-                              bf16 v_new and follow fast_p. */
+                              converts each bf16 value of v_new to fp16 (round
+                              to nearest even): exact for 2^-17 <= |v| <= 65504;
+                              smaller values round to a multiple of 2^-24
+                              (fp16's subnormal step; |v| <= 2^-25 becomes 0),
+                              an absolute error of at most 2^-25 that is not
+                              reported; a value beyond 65504 is reported by the
+                              next cpattn_sync_status as CPATTN_E_RANGE.
+                              Prefill then takes P in fp16 for cache tiles: one
+                              P.V product (11-bit P, relative RMS error about
+                              1.7e-3 on N(0,1) inputs, as the bf16 hi + lo
+                              pair) at the cost of fast_p.  Current-chunk tiles
+                              still read bf16 v_new and follow fast_p. */
+  int32_t pairing;         /* how prefill pairs adjacent q heads of one kv
+                              head when NQ/NKV is even (results meet the same
+                              accuracy in every form; the bits may differ):
+                              CPATTN_PAIRING_MMA2 (0, default): a CTA pair on
+                                the two SMs of a TPC runs 2-SM tensor-core MMAs
+                                (M = 256) and each SM stages half of every K/V
+                                tile;
+                              CPATTN_PAIRING_NONE: one CTA per (q head, row
+                                block);
+                              CPATTN_PAIRING_PINGPONG: HD = 128 only (MMA2 at
+                                HD = 256): one CTA holds both heads' query tiles
+                                and alternates their products with their
+                                softmaxes. */
+  int32_t gqa_packing;     /* CPATTN_GQA_PACKING_AUTO (0, default): launches
+                              whose chunks are all short run GQA-packed (see
+                              cpattn_prefill); CPATTN_GQA_PACKING_OFF: never */
 } cpattn_config;
+
+#define CPATTN_PAIRING_MMA2 0
+#define CPATTN_PAIRING_NONE 1
+#define CPATTN_PAIRING_PINGPONG 2
+#define CPATTN_GQA_PACKING_AUTO 0
+#define CPATTN_GQA_PACKING_OFF 1
 
 typedef struct cpattn_ctx cpattn_ctx; /* opaque */
 
@@ -89,20 +113,13 @@ typedef struct cpattn_ctx cpattn_ctx; /* opaque */
  * Allocates a few bytes of device memory for the timeout status word on the
  * current device (skipped, without error, when no device is present; launches
  * then fail with CPATTN_E_CUDA).
- * The environment variable CPATTN_PAIRING, read here, picks how prefill
- * pairs adjacent q heads of one kv head when NQ/NKV is even: "mma2"
- * (default: a CTA pair runs 2-SM tensor-core MMAs and each SM stages half of
- * every K/V tile), "multicast" (each CTA of a pair runs its own MMAs, the
- * pair shares K/V loads), "pingpong" (HD = 128: one CTA holds both heads'
- * query tiles and alternates their products with their softmaxes; "mma2" at
- * HD = 256), "none" (one CTA per unit).  Results meet the same accuracy in
- * every mode; the bits may differ between modes.
- * CPATTN_GQA_PACKING ("auto", the default, or "off"), also read here,
- * controls the packed form of short-chunk launches described at
- * cpattn_prefill.
- * Errors: E_INVALID (NULL, NQ % NKV != 0, sizes < 1, an unknown
- * CPATTN_PAIRING or CPATTN_GQA_PACKING), E_UNSUPPORTED (HD not 128/256),
- * E_NOMEM.
+ * The kernel form comes from cfg->pairing and cfg->gqa_packing.  For tests,
+ * the environment variables CPATTN_PAIRING ("mma2", "none", "pingpong") and
+ * CPATTN_GQA_PACKING ("auto", "off"), when set, override those two fields;
+ * they are read here.
+ * Errors: E_INVALID (NULL, NQ % NKV != 0, sizes < 1, a field out of range,
+ * an unknown CPATTN_PAIRING or CPATTN_GQA_PACKING value), E_UNSUPPORTED (HD
+ * not 128/256, NQ > 65535), E_NOMEM.
  */
 cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out);
 
@@ -271,6 +288,30 @@ cpattn_status cpattn_sync_status(cpattn_ctx* ctx, void* stream);
 cpattn_status cpattn_set_fault_injection(cpattn_ctx* ctx, int32_t flags, int32_t timeout_ms);
 
 /*
+ * Barrier accounting for tests (the PR's Design section: every signal must
+ * be matched by its wait, or the kernel deadlocks).  Only the barrier-count
+ * build of the library (compiled with -DCPATTN_COUNT_BARRIERS) implements
+ * it; other builds return E_UNSUPPORTED.  Once `records` is registered, every
+ * later prefill launch of this context adds, per CTA b (blockIdx), into
+ * records[b * CPATTN_COUNT_RECORD ..] (uint32):
+ *   row 0  [0, 40)    arrivals received by each mbarrier of CTA b (index =
+ *                     the kernel's barrier number), from either CTA of a pair
+ *   row 1  [40, 80)   completed waits of the softmax warps (one per warp)
+ *   row 2  [80, 120)  completed waits of the TMA producer
+ *   row 3  [120, 160) completed waits of the MMA warp
+ *   row 4  [160, 200) softmax waits for the previous tile's P.V before a
+ *                     rescale of O (data-dependent; apart from row 1)
+ * The caller zeroes the records before a launch and reads them after it.
+ * records: device memory, 4-byte aligned, at least (CTAs of the launch) *
+ * CPATTN_COUNT_RECORD * 4 bytes (a launch has at most one CTA per SM), else
+ * the prefill fails with E_INVALID; NULL turns counting off.
+ * Errors: E_INVALID (NULL ctx, misaligned records), E_UNSUPPORTED.
+ */
+#define CPATTN_COUNT_BARS 40
+#define CPATTN_COUNT_RECORD 200
+cpattn_status cpattn_set_barrier_counts(cpattn_ctx* ctx, void* records, uint64_t bytes);
+
+/*
  * Host-side view of the cache walk (no device work): for cache length L and
  * the context's P and S, writes the flat tile indices the prefill kernel
  * visits, in order, to tiles[0..n) and each tile's 128-column validity mask
@@ -301,7 +342,9 @@ cpattn_status cpattn_cache_walk_from(const cpattn_ctx* ctx, int32_t cache_len, i
  *
  * Same computation, arguments and layouts as cpattn_prefill, but it takes
  * the configuration directly instead of a context and never allocates: no
- * cudaMalloc, no cudaFree, no allocating library call, no host heap.  The
+ * cudaMalloc, no cudaFree, no allocating library call, no host heap.  It
+ * always runs the one-CTA-per-unit kernel form (cfg->pairing and
+ * cfg->gqa_packing are checked but not used) and never splits a walk.  The
  * kernel's bounded-wait status word lives in a file-scope device array of
  * CPATTN_NOALLOC_SCRATCH_INTS ints (256 bytes) that every GPU loading the
  * library keeps until process exit.

@@ -25,7 +25,13 @@ EXPORTS = ("cpattn_create", "cpattn_write_kv", "cpattn_prefill", "cpattn_sync_st
            "cpattn_set_fault_injection", "cpattn_cache_walk", "cpattn_destroy",
            "cpattn_status_string", "cpattn_last_error", "cpattn_prefill_noalloc",
            "cpattn_two_launch_workspace", "cpattn_prefill_two_launch", "cpattn_set_splitkv",
-           "cpattn_splitkv_workspace", "cpattn_cache_walk_from", "cpattn_prefill_write_kv")
+           "cpattn_splitkv_workspace", "cpattn_cache_walk_from", "cpattn_prefill_write_kv",
+           "cpattn_set_barrier_counts")
+
+# cpattn_config.pairing values, by name.
+PAIRING = {"mma2": 0, "none": 1, "pingpong": 2}
+COUNT_BARS = 40      # CPATTN_COUNT_BARS
+COUNT_RECORD = 200   # CPATTN_COUNT_RECORD: uint32 per CTA
 
 
 class CpattnError(RuntimeError):
@@ -39,17 +45,18 @@ class Config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("num_shards", ctypes.c_int32),
                 ("shard_capacity", ctypes.c_int32), ("chunk_size", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("fast_p", ctypes.c_int32),
-                ("v_cache_f16", ctypes.c_int32)]
+                ("v_cache_f16", ctypes.c_int32), ("pairing", ctypes.c_int32),
+                ("gqa_packing", ctypes.c_int32)]
 
 
-_lib = None
+_libs = {}
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load the library (once).  Raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
+    """Load a build of the library (once per path).  Raises if it has not
+    been built."""
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library {path} is missing: build it with "
                            "long_context_chunked_gb300.build.build()")
@@ -89,7 +96,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cpattn_cache_walk_from.restype = I32
     lib.cpattn_prefill_write_kv.argtypes = [P, I32, I32P, I32P, P, P, P, P, P, P, P, P]
     lib.cpattn_prefill_write_kv.restype = I32
-    _lib = lib
+    lib.cpattn_set_barrier_counts.argtypes = [P, P, ctypes.c_uint64]
+    lib.cpattn_set_barrier_counts.restype = I32
+    _libs[path] = lib
     return lib
 
 
@@ -117,14 +126,19 @@ def _stream(stream) -> int:
 
 
 class Context:
-    """One attention-layer shape: NQ, NKV, HD, shard count P, shard capacity S, chunk C."""
+    """One attention-layer shape: NQ, NKV, HD, shard count P, shard capacity S, chunk C.
+    pairing: "mma2" (default), "none" or "pingpong"; gqa_packing: False turns
+    the packed short-chunk form off; library: the path of another build of the
+    library (e.g. the barrier-count build) to run this context on."""
 
     def __init__(self, num_q_heads: int, num_kv_heads: int, head_dim: int, num_shards: int,
                  shard_capacity: int, chunk_size: int, softmax_scale: float = 0.0,
-                 fast_p: bool = False, v_cache_f16: bool = False):
-        self.lib = load()
+                 fast_p: bool = False, v_cache_f16: bool = False, pairing: str = "mma2",
+                 gqa_packing: bool = True, library: Optional[str] = None):
+        self.lib = load(library or LIB_PATH)
         self.cfg = Config(num_q_heads, num_kv_heads, head_dim, num_shards, shard_capacity,
-                          chunk_size, softmax_scale, int(bool(fast_p)), int(bool(v_cache_f16)))
+                          chunk_size, softmax_scale, int(bool(fast_p)), int(bool(v_cache_f16)),
+                          PAIRING[pairing], 0 if gqa_packing else 1)
         self.v_cache_f16 = bool(v_cache_f16)
         h = ctypes.c_void_p()
         st = self.lib.cpattn_create(ctypes.byref(self.cfg), ctypes.byref(h))
@@ -133,9 +147,11 @@ class Context:
         self._h = h
 
     @classmethod
-    def for_workload(cls, w, fast_p: bool = False, v_cache_f16: bool = False) -> "Context":
+    def for_workload(cls, w, fast_p: bool = False, v_cache_f16: bool = False,
+                     pairing: str = "mma2", gqa_packing: bool = True,
+                     library: Optional[str] = None) -> "Context":
         return cls(w.num_q_heads, w.num_kv_heads, w.head_dim, w.shards, w.shard_capacity,
-                   w.chunk, w.scale, fast_p, v_cache_f16)
+                   w.chunk, w.scale, fast_p, v_cache_f16, pairing, gqa_packing, library)
 
     # -- status --------------------------------------------------------
     def _check(self, st: int):
@@ -224,6 +240,12 @@ class Context:
     def sync_status(self, stream=None) -> int:
         """Synchronise and return the status code (E_TIMEOUT if a device wait expired)."""
         return self.lib.cpattn_sync_status(self._h, _stream(stream))
+
+    def set_barrier_counts(self, records=None):
+        """Register a zeroed device uint32 tensor of COUNT_RECORD entries per
+        CTA (barrier-count build only), or None to stop counting."""
+        nbytes = 0 if records is None else records.numel() * records.element_size()
+        self._check(self.lib.cpattn_set_barrier_counts(self._h, _ptr(records), nbytes))
 
     def set_fault_injection(self, flags: int, timeout_ms: int = 0):
         self._check(self.lib.cpattn_set_fault_injection(self._h, flags, timeout_ms))

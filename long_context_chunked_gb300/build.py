@@ -13,6 +13,11 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libcpattn.so")
 # Race-detection build: MMA groups serialised (see CPATTN_SERIALIZE_MMA).
 LIB_SERIALIZED = os.path.join(PKG, "libcpattn_serialized.so")
+# Barrier-count build: every mbarrier arrival and wait counted (see
+# CPATTN_COUNT_BARRIERS and cpattn_set_barrier_counts).
+LIB_COUNTED = os.path.join(PKG, "libcpattn_counted.so")
+VARIANTS = {"release": (LIB, []), "serialized": (LIB_SERIALIZED, ["-DCPATTN_SERIALIZE_MMA"]),
+            "counted": (LIB_COUNTED, ["-DCPATTN_COUNT_BARRIERS"])}
 SOURCES = ["cpattn.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
@@ -33,21 +38,19 @@ def _stale(lib: str) -> bool:
 
 
 def build_all(force: bool = False) -> None:
-    """Both variants, compiled concurrently."""
+    """Every variant, compiled concurrently."""
     import concurrent.futures as cf
-    with cf.ThreadPoolExecutor(2) as ex:
-        for f in [ex.submit(build, force, False, False), ex.submit(build, force, False, True)]:
+    with cf.ThreadPoolExecutor(len(VARIANTS)) as ex:
+        for f in [ex.submit(build, force, False, v) for v in VARIANTS]:
             f.result()
 
 
-def build(force: bool = False, verbose: bool = False, serialized: bool = False) -> str:
-    lib = LIB_SERIALIZED if serialized else LIB
+def build(force: bool = False, verbose: bool = False, variant: str = "release") -> str:
+    lib, defines = VARIANTS[variant]
     if not force and not _stale(lib):
         return lib
     cmd = [nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I" + INCLUDE, "-o", lib + ".tmp"] + [os.path.join(CSRC, s) for s in SOURCES]
-    if serialized:
-        cmd.insert(2, "-DCPATTN_SERIALIZE_MMA")
+           "-I" + INCLUDE, "-o", lib + ".tmp"] + defines + [os.path.join(CSRC, s) for s in SOURCES]
     if verbose:
         cmd.insert(2, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -60,5 +63,5 @@ def build(force: bool = False, verbose: bool = False, serialized: bool = False) 
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                serialized="--serialized" in sys.argv))
+    variant = next((v for v in VARIANTS if "--" + v in sys.argv), "release")
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, variant=variant))

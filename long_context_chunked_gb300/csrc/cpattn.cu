@@ -23,23 +23,34 @@
 #include "merge.cuh"
 #include "plan.h"
 
+static_assert(cpattn::kCountRecord == CPATTN_COUNT_RECORD && cpattn::kCountBars == CPATTN_COUNT_BARS,
+              "barrier-count record layout");
+static_assert(cpattn::Layout<128>::NBAR <= cpattn::kCountBars &&
+                  cpattn::Layout<256>::NBAR <= cpattn::kCountBars &&
+                  cpattn::PingPongLayout::NBAR <= cpattn::kCountBars,
+              "every barrier has a count slot");
+
 struct cpattn_ctx {
   cpattn_config cfg;
   int device = -1;
   int num_sms = 0;
   int* d_status = nullptr;           // device status word (timeouts)
   int grid_cap[2][2][4][2] = {};  // [HD == 256][split P][pairing mode][fp16 V cache]: 0 until set up
-  // Head pairing for even group sizes (CPATTN_PAIRING = mma2 | multicast |
-  // pingpong | none): 2 = 2-SM MMA pairs, 1 = CTA pairs sharing K/V loads by
-  // multicast, 3 = two query tiles per CTA (HD = 128; 2 at HD = 256), 0 = off.
+  // Head pairing for even group sizes (cpattn_config.pairing, or the
+  // CPATTN_PAIRING override): 2 = 2-SM MMA pairs, 3 = two query tiles per CTA
+  // (HD = 128; 2 at HD = 256), 0 = off.
   int pair_mode = 2;
   // Split-KV: a caller-owned device workspace and the policy (kSplitOff,
   // kSplitAuto, or a forced piece length in tiles); off until registered.
   void* split_ws = nullptr;
   size_t split_ws_bytes = 0;
   int split_policy = cpattn::kSplitOff;
-  // GQA packing for short-chunk launches (CPATTN_GQA_PACKING = auto | off).
+  // GQA packing for short-chunk launches (cpattn_config.gqa_packing, or the
+  // CPATTN_GQA_PACKING override).
   bool gqa_packing = true;
+  // Barrier-count build: caller-owned per-CTA count records, and their bytes.
+  uint32_t* bar_counts = nullptr;
+  size_t bar_counts_bytes = 0;
   int debug_flags = 0;
   unsigned long long timeout_ns = 1000ull * 1000 * 1000;
   bool debug_sync = false;
@@ -130,8 +141,9 @@ cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* wha
 
 template <int HD, bool SPLIT, int MODE, bool VF16>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
-  static_assert(MODE != 3 || HD == 128, "two query tiles per CTA only at HD = 128");
-  constexpr bool MC = MODE == 1 || MODE == 2;  // launched as clusters of two CTAs
+  static_assert(MODE == 0 || MODE == 2 || (MODE == 3 && HD == 128),
+                "pairing modes: 0 (none), 2 (2-SM MMA pairs), 3 (two query tiles, HD = 128)");
+  constexpr bool MC = MODE == 2;  // launched as clusters of two CTAs
   constexpr int SMEM_BYTES =
       MODE == 3 ? cpattn::PingPongLayout::SMEM_BYTES : cpattn::Layout<HD>::SMEM_BYTES;
   void (*kernel)(cpattn::PrefillParams);
@@ -140,7 +152,7 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
   else if constexpr (MODE == 2)
     kernel = cpattn::prefill_kernel_pair2<HD, SPLIT, VF16>;
   else
-    kernel = cpattn::prefill_kernel<HD, SPLIT, MODE == 1, VF16>;
+    kernel = cpattn::prefill_kernel<HD, SPLIT, VF16>;
   int& grid_cap = ctx->grid_cap[HD == 256][SPLIT][MODE][VF16];
   if (grid_cap == 0) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -172,6 +184,13 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
   // A CTA of MODE 3 takes two units (a head pair) per round.
   int grid = std::min(MODE == 3 ? prm->num_units / 2 : prm->num_units, grid_cap);
   if (MC) grid &= ~1;
+  if (ctx->bar_counts != nullptr) {
+    if (ctx->bar_counts_bytes < static_cast<size_t>(grid) * cpattn::kCountRecord * 4)
+      return fail(ctx, CPATTN_E_INVALID,
+                  "the barrier-count buffer holds fewer records than the launch's " +
+                      std::to_string(grid) + " CTAs");
+    prm->bar_counts = ctx->bar_counts;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(cpattn::kThreads, 1, 1);
@@ -210,7 +229,7 @@ void plan_shape(const cpattn_ctx* ctx, bool packed, int* executors, int* units_p
     return;
   }
   const int mode = launch_pair_mode(ctx, packed);
-  *executors = (mode == 1 || mode == 2) ? sms / 2 : sms;
+  *executors = mode == 2 ? sms / 2 : sms;
   *units_per_block = mode != 0 ? ctx->cfg.num_q_heads / 2 : ctx->cfg.num_q_heads;
 }
 
@@ -238,8 +257,6 @@ cpattn_status dispatch_prefill_hd(cpattn_ctx* ctx, cpattn::PrefillParams* prm, c
   }
   if (mode == 2) return split ? launch_prefill<HD, true, 2, VF16>(ctx, prm, st)
                               : launch_prefill<HD, false, 2, VF16>(ctx, prm, st);
-  if (mode == 1) return split ? launch_prefill<HD, true, 1, VF16>(ctx, prm, st)
-                              : launch_prefill<HD, false, 1, VF16>(ctx, prm, st);
   return split ? launch_prefill<HD, true, 0, VF16>(ctx, prm, st)
                : launch_prefill<HD, false, 0, VF16>(ctx, prm, st);
 }
@@ -414,26 +431,42 @@ const char* cpattn_last_error(const cpattn_ctx* ctx) {
   return ctx == nullptr ? "" : ctx->last_error.c_str();
 }
 
+// Checks of a configuration shared by cpattn_create and the allocation-free
+// prefill.
+static cpattn_status check_config(const cpattn_config& c) {
+  if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
+      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1 ||
+      c.v_cache_f16 < 0 || c.v_cache_f16 > 1 || c.pairing < 0 || c.pairing > 2 ||
+      c.gqa_packing < 0 || c.gqa_packing > 1)
+    return CPATTN_E_INVALID;
+  if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
+  // Work units are (row block, q head) and their count must fit the kernel's int.
+  if (c.num_q_heads > 65535) return CPATTN_E_UNSUPPORTED;
+  return CPATTN_OK;
+}
+
 cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   if (out == nullptr || cfg == nullptr) return CPATTN_E_INVALID;
   *out = nullptr;
   const cpattn_config& c = *cfg;
-  if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
-      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1 ||
-      c.v_cache_f16 < 0 || c.v_cache_f16 > 1)
-    return CPATTN_E_INVALID;
-  if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
-  if (c.num_q_heads > 65535) return CPATTN_E_UNSUPPORTED;
+  const cpattn_status cs = check_config(c);
+  if (cs != CPATTN_OK) return cs;
   cpattn_ctx* ctx = new (std::nothrow) cpattn_ctx();
   if (ctx == nullptr) return CPATTN_E_NOMEM;
   ctx->cfg = c;
   if (!(c.softmax_scale > 0.f)) ctx->cfg.softmax_scale = 1.0f / std::sqrt(static_cast<float>(c.head_dim));
+  ctx->pair_mode = c.pairing == CPATTN_PAIRING_NONE       ? 0
+                   : c.pairing == CPATTN_PAIRING_PINGPONG ? 3
+                                                          : 2;
+  ctx->gqa_packing = c.gqa_packing == CPATTN_GQA_PACKING_AUTO;
   const char* dbg = std::getenv("CPATTN_DEBUG");
   ctx->debug_sync = dbg != nullptr && dbg[0] == '1';
+  // Test overrides of the configuration's kernel-form fields.
   const char* packing = std::getenv("CPATTN_GQA_PACKING");
   if (packing != nullptr) {
     if (std::strcmp(packing, "off") == 0) ctx->gqa_packing = false;
-    else if (std::strcmp(packing, "auto") != 0) {
+    else if (std::strcmp(packing, "auto") == 0) ctx->gqa_packing = true;
+    else {
       delete ctx;
       return CPATTN_E_INVALID;
     }
@@ -441,7 +474,6 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   const char* pairing = std::getenv("CPATTN_PAIRING");
   if (pairing != nullptr) {
     if (std::strcmp(pairing, "none") == 0) ctx->pair_mode = 0;
-    else if (std::strcmp(pairing, "multicast") == 0) ctx->pair_mode = 1;
     else if (std::strcmp(pairing, "mma2") == 0) ctx->pair_mode = 2;
     else if (std::strcmp(pairing, "pingpong") == 0) ctx->pair_mode = 3;
     else {
@@ -478,6 +510,20 @@ cpattn_status cpattn_set_fault_injection(cpattn_ctx* ctx, int32_t flags, int32_t
   ctx->timeout_ns = timeout_ms > 0 ? static_cast<unsigned long long>(timeout_ms) * 1000000ull
                                    : 1000ull * 1000 * 1000;
   return CPATTN_OK;
+}
+
+cpattn_status cpattn_set_barrier_counts(cpattn_ctx* ctx, void* records, uint64_t bytes) {
+  if (ctx == nullptr) return CPATTN_E_INVALID;
+#ifdef CPATTN_COUNT_BARRIERS
+  if (records != nullptr && (reinterpret_cast<uintptr_t>(records) & 3u) != 0)
+    return fail(ctx, CPATTN_E_INVALID, "barrier-count records must be 4-byte aligned");
+  ctx->bar_counts = static_cast<uint32_t*>(records);
+  ctx->bar_counts_bytes = records != nullptr ? static_cast<size_t>(bytes) : 0;
+  return CPATTN_OK;
+#else
+  (void)records, (void)bytes;
+  return fail(ctx, CPATTN_E_UNSUPPORTED, "barrier counting needs the barrier-count build");
+#endif
 }
 
 cpattn_status cpattn_cache_walk(const cpattn_ctx* ctx, int32_t cache_len, int32_t* tiles,
@@ -752,13 +798,13 @@ constexpr int kNoAllocMaxDevices = 64;
 // point launches it (plain launch, no cluster).
 template <int HD, bool SPLIT, bool VF16>
 cudaError_t noalloc_attr() {
-  return cudaFuncSetAttribute(cpattn::prefill_kernel<HD, SPLIT, false, VF16>,
+  return cudaFuncSetAttribute(cpattn::prefill_kernel<HD, SPLIT, VF16>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               cpattn::Layout<HD>::SMEM_BYTES);
 }
 template <int HD, bool SPLIT, bool VF16>
 void noalloc_launch(int grid, cudaStream_t st, const cpattn::PrefillParams& prm) {
-  cpattn::prefill_kernel<HD, SPLIT, false, VF16>
+  cpattn::prefill_kernel<HD, SPLIT, VF16>
       <<<grid, cpattn::kThreads, cpattn::Layout<HD>::SMEM_BYTES, st>>>(prm);
 }
 
@@ -824,11 +870,8 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
                                                 void* out, float* lse, void* stream) {
   if (cfg == nullptr) return CPATTN_E_INVALID;
   const cpattn_config& c = *cfg;
-  if (c.num_q_heads < 1 || c.num_kv_heads < 1 || c.num_shards < 1 || c.shard_capacity < 1 ||
-      c.chunk_size < 1 || c.num_q_heads % c.num_kv_heads != 0 || c.fast_p < 0 || c.fast_p > 1 ||
-      c.v_cache_f16 < 0 || c.v_cache_f16 > 1)
-    return CPATTN_E_INVALID;
-  if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
+  const cpattn_status cs = check_config(c);
+  if (cs != CPATTN_OK) return cs;
   // Fixed-capacity host tables: sizes beyond them are refused, not grown.
   if (num_seqs < 1) return CPATTN_E_INVALID;
   if (num_seqs > CPATTN_MAX_SEQS) return CPATTN_E_UNSUPPORTED;

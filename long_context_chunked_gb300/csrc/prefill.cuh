@@ -79,6 +79,8 @@ struct PrefillParams {
   const __nv_bfloat16* v_new;
   __nv_bfloat16* k_cache_w;
   __nv_bfloat16* v_cache_w;
+  // Barrier-count build only: kCountRecord uint32 per CTA (see ptx.cuh), or null.
+  uint32_t* bar_counts;
   float* ws_o;    // split-KV pieces: fp32 O / l, [partial rows][NQ][HD]
   float* ws_lse;  // split-KV pieces: LSE, [partial rows][NQ]
   SeqInfo seqs[CPATTN_MAX_SEQS];
@@ -198,6 +200,16 @@ __device__ __forceinline__ int unit_of(int r) {
   return r * static_cast<int>(gridDim.x) + slot * PAIR + rank;
 }
 
+// The bounded wait of the role that warp `warp` runs (its count row in the
+// barrier-count build); bar0 is the shared address of barrier 0.
+__device__ __forceinline__ BoundedWait make_wait(volatile int* abort_flag, const PrefillParams& p,
+                                                 uint32_t bar0, int warp) {
+  const int row = warp < kSoftmaxWarps    ? kCountRowSoftmax
+                  : warp == kProducerWarp ? kCountRowProducer
+                                          : kCountRowMma;
+  return BoundedWait{abort_flag, p.status, p.timeout_ns, p.bar_counts, bar0, row};
+}
+
 // Ring position shared by producer and consumer.
 struct RingPos {
   int slot = 0;
@@ -220,7 +232,7 @@ namespace cpattn {
 constexpr unsigned long long kDrainLimitNs = 200ull * 1000 * 1000;
 
 // ------------------------------------------------------------- TMA producer
-template <int HD, bool MC>
+template <int HD>
 __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t sbase,
                                               const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -230,48 +242,34 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
   uint32_t q_issued = 0;
   bool ok = true;
 
-  // Paired CTAs (MC): both walk the same K/V tiles for two q heads of one kv
-  // head; each loads half of every sub-tile and multicasts it into the same
-  // slot of both CTAs, so every tile leaves L2 once per pair.  A slot is
-  // refilled only after both CTAs' MMAs released it (its empty barrier
-  // counts one multicast commit from each).
-  const int rank = MC ? static_cast<int>(cluster_ctarank()) : 0;
-
   // One 16 KB ring slot: wait until the slot is free, expect its 16 KB,
-  // then issue this CTA's boxes (`nbox` boxes of 64 columns from column x0;
-  // with MC the K half-tile rows or half of the V column boxes).
-  auto load_sub = [&](bool is_k, const CUtensorMap* m, const CUtensorMap* m_half, int x0, int y,
-                      int z) {
+  // then issue its boxes (a K sub-tile is one 64-column box of the 128-row
+  // tile; a V sub-tile is KCH boxes of VROWS rows).
+  auto load_sub = [&](bool is_k, const CUtensorMap* m, int y, int z, int x0) {
     if (rp.round && !wait(bar(Ly::B_SLOTEMPTY + rp.slot), rp.phase ^ 1u, kSiteSlotEmpty))
       return false;
     const uint32_t full = bar(Ly::B_SLOTFULL + rp.slot);
+    count_arrive(p.bar_counts, 1u, Ly::B_SLOTFULL + rp.slot, 1);
     mbar_arrive_expect_tx(full, Ly::SUB);
     const uint32_t dst = sbase + Ly::OFF_RING + static_cast<uint32_t>(rp.slot) * Ly::SUB;
     if (is_k) {
-      if (MC)
-        tma_load_3d_mc(dst + rank * (Ly::SUB / 2), m_half, full, x0, y, z + rank * (kBKV / 2), 0x3);
-      else
-        tma_load_3d(dst, m, full, x0, y, z);
+      tma_load_3d(dst, m, full, x0, y, z);
     } else {
       constexpr int BOX = Ly::VROWS * 128;
-      if (MC) {
-        for (int i = rank * (Ly::KCH / 2); i < (rank + 1) * (Ly::KCH / 2); ++i)
-          tma_load_3d_mc(dst + i * BOX, m, full, 64 * i, y, z, 0x3);
-      } else {
-        for (int i = 0; i < Ly::KCH; ++i) tma_load_3d(dst + i * BOX, m, full, 64 * i, y, z);
-      }
+      for (int i = 0; i < Ly::KCH; ++i) tma_load_3d(dst + i * BOX, m, full, 64 * i, y, z);
     }
     rp.template advance<Ly::NSLOT>();
     ++issued;
     return true;
   };
 
-  for (int ur = 0, u = unit_of<MC ? 2 : 1>(0); ok && u < p.num_units; u = unit_of<MC ? 2 : 1>(++ur)) {
+  for (int ur = 0, u = unit_of<1>(0); ok && u < p.num_units; u = unit_of<1>(++ur)) {
     const Unit U = decode_unit(p, u);
     if (q_issued > 0 && !wait(bar(Ly::B_QEMPTY), (q_issued - 1) & 1u, kSiteQEmpty)) {
       ok = false;
       break;
     }
+    count_arrive(p.bar_counts, 1u, Ly::B_QFULL, 1);
     mbar_arrive_expect_tx(bar(Ly::B_QFULL), Ly::Q_BYTES);
     for (int c = 0; c < Ly::KCH; ++c)
       tma_load_3d(sbase + Ly::OFF_Q + c * (kBQ * 128), p.packed ? &p.tm_q_packed : &p.tm_q,
@@ -288,11 +286,10 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
       const bool in_cache = v < U.n_cache;
       const int tile = in_cache ? wk.next() : 0;
       const CUtensorMap* m = in_cache ? &p.tm_k_cache : &p.tm_k_new;
-      const CUtensorMap* mh = in_cache ? &p.tm_k_cache_h : &p.tm_k_new_h;
       const int y = in_cache ? 0 : U.g;
       const int z = in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV;
       for (int c = 0; c < Ly::KCH; ++c)
-        if (!load_sub(true, m, mh, 64 * c, y, z)) return false;
+        if (!load_sub(true, m, y, z, 64 * c)) return false;
       return true;
     };
     auto load_v = [&](int v) {
@@ -302,7 +299,7 @@ __device__ __forceinline__ void producer_role(const PrefillParams& p, uint32_t s
       const int y = in_cache ? 0 : U.g;
       const int z = in_cache ? head_row + tile * kBKV : U.b * p.C + (v - U.n_cache) * kBKV;
       for (int j = 0; j < Ly::VSUB; ++j)
-        if (!load_sub(false, m, m, 0, y, z + j * Ly::VROWS)) return false;
+        if (!load_sub(false, m, y, z + j * Ly::VROWS, 0)) return false;
       return true;
     };
     // This block's slice of the walk starts at virtual tile U.v0.
@@ -371,7 +368,7 @@ __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane)
 // Run by the whole MMA warp: control flow and operands are warp-uniform (every
 // wait's outcome is agreed by the warp), and each MMA and commit is issued by
 // one elected lane.
-template <int HD, bool SPLIT, bool MC, bool VF16>
+template <int HD, bool SPLIT, bool VF16>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                          const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -384,9 +381,10 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   auto wwait = [&](uint32_t b, uint32_t parity, int site) {
     return __all_sync(0xFFFFFFFFu, wait(b, parity, site));
   };
-  // A slot is released to the producers of every CTA that shares it.
-  auto release_slot = [](uint32_t b) {
-    if (MC) mma_commit_mc(b, 0x3); else mma_commit(b);
+  // Commit (arrive once on barrier i when every MMA issued so far is done).
+  auto commit = [&](int i) {
+    count_commit(p.bar_counts, 1u, i);
+    mma_commit(bar(i));
   };
 #ifdef CPATTN_SERIALIZE_MMA
   // Race-detection build: every MMA group completes before the MMA thread
@@ -394,8 +392,9 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   // A correct protocol gives the same results bit for bit.
   uint32_t ser_phase = 0;
   auto serialize = [&]() {
-    mma_commit(bar(Ly::B_DRAIN));
+    commit(Ly::B_DRAIN);
     mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+    count_wait(p.bar_counts, kCountRowMma, Ly::B_DRAIN);
     ser_phase ^= 1u;
   };
 #else
@@ -433,10 +432,10 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
         }
       }
       serialize();
-      release_slot(bar(Ly::B_SLOTEMPTY + rp.slot));
+      commit(Ly::B_SLOTEMPTY + rp.slot);
       rp.template advance<Ly::NSLOT>();
     }
-    mma_commit(bar(Ly::B_ODONE + static_cast<int>(t & 1u)));
+    commit(Ly::B_ODONE + static_cast<int>(t & 1u));
     return true;
   };
   auto issue_pv = [&](const Unit& U, int w, uint32_t t) {
@@ -446,7 +445,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
     return issue_pv_as(w, t, std::false_type{});
   };
 
-  for (int ur = 0, u = unit_of<MC ? 2 : 1>(0); ok && u < p.num_units; u = unit_of<MC ? 2 : 1>(++ur), ++units) {
+  for (int ur = 0, u = unit_of<1>(0); ok && u < p.num_units; u = unit_of<1>(++ur), ++units) {
     const Unit U = decode_unit(p, u);
     if (!wwait(bar(Ly::B_QFULL), units & 1u, kSiteQFull)) {
       ok = false;
@@ -470,12 +469,12 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
           mma_ss(s_tmem, ad, bd, Ly::IDESC_QK, (c | kk) != 0);
         }
         serialize();
-        release_slot(bar(Ly::B_SLOTEMPTY + rp.slot));
+        commit(Ly::B_SLOTEMPTY + rp.slot);
         rp.template advance<Ly::NSLOT>();
       }
       if (!ok) break;
-      mma_commit(bar(Ly::B_SFULL + sb));
-      if (v == U.n_tiles - 1) mma_commit(bar(Ly::B_QEMPTY));
+      commit(Ly::B_SFULL + sb);
+      if (v == U.n_tiles - 1) commit(Ly::B_QEMPTY);
       if (v >= 1 && !issue_pv(U, v - 1, tile_ctr - 1)) {
         ok = false;
         break;
@@ -485,8 +484,9 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
     if (ok) ok = issue_pv(U, U.n_tiles - 1, tile_ctr - 1);
   }
   // Every MMA issued must complete before TMEM is released.
-  mma_commit(bar(Ly::B_DRAIN));
-  mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+  commit(Ly::B_DRAIN);
+  if (mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs))
+    count_wait(p.bar_counts, kCountRowMma, Ly::B_DRAIN);
 }
 }  // namespace cpattn
 
@@ -612,6 +612,9 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
   const float sl2 = p.scale_log2;
   uint32_t tile_ctr = 0;
   bool drop_one = (p.debug_flags & kDebugDropArrive) && blockIdx.x == 0 && threadIdx.x == 0;
+  // The wait for the previous tile's P.V before a rescale of O, counted apart
+  // from the in-order waits in the barrier-count build.
+  const BoundedWait wait_rescale = wait.with_row(kCountRowRescale);
   constexpr int OCOLS = HD / NG;                        // O columns of this group
 
   for (int ur = 0, u = unit_of<CL>(0); u < p.num_units; u = unit_of<CL>(++ur)) {
@@ -750,15 +753,15 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       // at most one phase behind; with the two barriers and PV of tile t held
       // back by this thread's arrival below, that always holds.  Only a tile
       // that rescales O also waits for PV of tile t-1.
-      auto pv_wait = [&](uint32_t t) {
-        return wait(bar(Ly::B_ODONE + static_cast<int>(t & 1u)), (t >> 1) & 1u, kSiteODone);
+      auto pv_wait = [&](const BoundedWait& w, uint32_t t) {
+        return w(bar(Ly::B_ODONE + static_cast<int>(t & 1u)), (t >> 1) & 1u, kSiteODone);
       };
       if (tile_ctr >= 2) {
-        ok = __all_sync(0xFFFFFFFFu, pv_wait(tile_ctr - 2));
+        ok = __all_sync(0xFFFFFFFFu, pv_wait(wait, tile_ctr - 2));
         if (!ok) *pair_fail = 1;  // acted on at the next pair barrier
       }
       if (ok && warp_rescale) {
-        ok = __all_sync(0xFFFFFFFFu, pv_wait(tile_ctr - 1));
+        ok = __all_sync(0xFFFFFFFFu, pv_wait(wait_rescale, tile_ctr - 1));
         if (!ok) *pair_fail = 1;
         tc_fence_after();
         if (ok) {
@@ -777,14 +780,17 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       if (PAIR2) {
         __syncwarp();
         if ((threadIdx.x & 31) == 0) {
-          if (drop_one)
+          if (drop_one) {
             drop_one = false;  // fault-injection hook: this arrival never happens
-          else
+          } else {
+            count_arrive(p.bar_counts, 1u, Ly::B_PFULL + sb, 1);  // the leader's barrier
             mbar_arrive_remote(mapa_shared(bar(Ly::B_PFULL + sb), 0));
+          }
         }
       } else if (drop_one) {
         drop_one = false;  // fault-injection hook: this arrival never happens
       } else {
+        count_arrive(p.bar_counts, 1u, Ly::B_PFULL + sb, 1);
         mbar_arrive(bar(Ly::B_PFULL + sb));
       }
       ++tile_ctr;
@@ -816,7 +822,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 }
 
 // ------------------------------------------------------------------ kernel
-template <int HD, bool SPLIT, bool MC, bool VF16>
+template <int HD, bool SPLIT, bool VF16>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -834,9 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Ly::NBAR; ++i)
-      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? kSoftmaxThreads
-                        : (MC && i >= Ly::B_SLOTEMPTY)                ? 2u
-                                                                      : 1u);
+      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? kSoftmaxThreads : 1u);
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) reinterpret_cast<volatile int*>(smem + Ly::OFF_PFAIL)[i] = 0;
     fence_mbar_init();
@@ -847,31 +851,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     prefetch_tmap(&p.tm_v_new);
     prefetch_tmap(&p.tm_k_cache);
     prefetch_tmap(&p.tm_v_cache);
-    if (MC) {
-      prefetch_tmap(&p.tm_k_new_h);
-      prefetch_tmap(&p.tm_k_cache_h);
-    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), Ly::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
-  // With MC the peer multicasts into this CTA's slots and barriers: no copy
-  // may start before both CTAs initialised their barriers.
-  if (MC) cluster_sync(); else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
+  const BoundedWait wait = make_wait(abort_flag, p, bar(0), warp);
 
   if (warp < kProducerWarp) {
-    softmax_role<HD, SPLIT, false, VF16, MC ? 2 : 1>(p, sbase, tmem, wait);
+    softmax_role<HD, SPLIT, false, VF16, 1>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<HD, MC>(p, sbase, wait);
+    if (lane == 0) producer_role<HD>(p, sbase, wait);
   } else if (warp == kWriterWarp) {
-    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, MC ? 2 : 1>(p, lane);
+    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 1>(p, lane);
   } else {
-    mma_role<HD, SPLIT, MC, VF16>(p, sbase, tmem, wait);
+    mma_role<HD, SPLIT, VF16>(p, sbase, tmem, wait);
   }
   __syncwarp();
   tc_fence_before();
@@ -880,8 +878,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_after();
     tmem_dealloc(tmem, Ly::TMEM_COLS);
   }
-  // Neither CTA of a pair leaves while the other may still write into it.
-  if (MC) cluster_sync();
 }
 
 }  // namespace cpattn

@@ -74,6 +74,7 @@ __device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint
     if (rp.round && !wait(bar(Ly::B_SLOTEMPTY + rp.slot), rp.phase ^ 1u, kSiteSlotEmpty))
       return false;
     const uint32_t full = lead(Ly::B_SLOTFULL + rp.slot);
+    count_arrive(p.bar_counts, 1u, Ly::B_SLOTFULL + rp.slot, 1);
     mbar_arrive_expect_tx_remote(full, Ly::SUB);
     emit(sbase + Ly::OFF_RING + static_cast<uint32_t>(rp.slot) * Ly::SUB, full);
     rp.template advance<Ly::NSLOT>();
@@ -88,6 +89,7 @@ __device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint
       break;
     }
     const uint32_t qfull = lead(Ly::B_QFULL);
+    count_arrive(p.bar_counts, 1u, Ly::B_QFULL, 1);
     mbar_arrive_expect_tx_remote(qfull, Ly::Q_BYTES);
     for (int c = 0; c < Ly::KCH; ++c)
       tma_load_3d_pair(sbase + Ly::OFF_Q + c * (kBQ * 128), &p.tm_q, qfull, 64 * c, U.h,
@@ -174,13 +176,20 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
   auto wwait = [&](uint32_t b, uint32_t parity, int site) {
     return __all_sync(0xFFFFFFFFu, wait(b, parity, site));
   };
+  // Commit of the leader's MMAs so far, arriving on barrier i of the CTAs in
+  // cta_mask (0x3: both, 0x1: the leader).
+  auto commit = [&](int i, uint16_t cta_mask) {
+    count_commit(p.bar_counts, cta_mask, i);
+    mma2_commit_mc(bar(i), cta_mask);
+  };
 #ifdef CPATTN_SERIALIZE_MMA
   // Race-detection build: every MMA group completes before the MMA thread
   // moves on (see prefill.cuh).
   uint32_t ser_phase = 0;
   auto serialize = [&]() {
-    mma2_commit_mc(bar(Ly::B_DRAIN), 0x1);
+    commit(Ly::B_DRAIN, 0x1);
     mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+    count_wait(p.bar_counts, kCountRowMma, Ly::B_DRAIN);
     ser_phase ^= 1u;
   };
 #else
@@ -217,10 +226,10 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
         }
       }
       serialize();
-      mma2_commit_mc(bar(Ly::B_SLOTEMPTY + rp.slot), 0x3);
+      commit(Ly::B_SLOTEMPTY + rp.slot, 0x3);
       rp.template advance<Ly::NSLOT>();
     }
-    mma2_commit_mc(bar(Ly::B_ODONE + static_cast<int>(t & 1u)), 0x3);
+    commit(Ly::B_ODONE + static_cast<int>(t & 1u), 0x3);
     return true;
   };
   auto issue_pv = [&](const Unit& U, int w, uint32_t t) {
@@ -258,12 +267,12 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
           }
         }
         serialize();
-        mma2_commit_mc(bar(Ly::B_SLOTEMPTY + rp.slot), 0x3);
+        commit(Ly::B_SLOTEMPTY + rp.slot, 0x3);
         rp.template advance<Ly::NSLOT>();
       }
       if (!ok) break;
-      mma2_commit_mc(bar(Ly::B_SFULL + sb), 0x3);
-      if (v == U.n_tiles - 1) mma2_commit_mc(bar(Ly::B_QEMPTY), 0x3);
+      commit(Ly::B_SFULL + sb, 0x3);
+      if (v == U.n_tiles - 1) commit(Ly::B_QEMPTY, 0x3);
       if (v >= 1 && !issue_pv(U, v - 1, tile_ctr - 1)) {
         ok = false;
         break;
@@ -273,8 +282,9 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
     if (ok) ok = issue_pv(U, U.n_tiles - 1, tile_ctr - 1);
   }
   // Every MMA issued must complete before either CTA releases its TMEM.
-  mma2_commit_mc(bar(Ly::B_DRAIN), 0x1);
-  mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+  commit(Ly::B_DRAIN, 0x1);
+  if (mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs))
+    count_wait(p.bar_counts, kCountRowMma, Ly::B_DRAIN);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -329,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
+  const BoundedWait wait = make_wait(abort_flag, p, bar(0), warp);
 
   if (warp < kProducerWarp) {
     softmax_role<HD, SPLIT, true, VF16, 2>(p, sbase, tmem, wait);

@@ -97,6 +97,7 @@ __device__ __forceinline__ void producer_role_pingpong(const PrefillParams& p, u
     if (rp.round && !wait(bar(Ly::B_SLOTEMPTY + rp.slot), rp.phase ^ 1u, kSiteSlotEmpty))
       return false;
     const uint32_t full = bar(Ly::B_SLOTFULL + rp.slot);
+    count_arrive(p.bar_counts, 1u, Ly::B_SLOTFULL + rp.slot, 1);
     mbar_arrive_expect_tx(full, Ly::SUB);
     const uint32_t dst = sbase + Ly::OFF_RING + static_cast<uint32_t>(rp.slot) * Ly::SUB;
     for (int i = 0; i < nbox; ++i) tma_load_3d(dst + i * box, m, full, x0 + 64 * i, y, z);
@@ -111,6 +112,7 @@ __device__ __forceinline__ void producer_role_pingpong(const PrefillParams& p, u
       ok = false;
       break;
     }
+    count_arrive(p.bar_counts, 1u, Ly::B_QFULL, 1);
     mbar_arrive_expect_tx(bar(Ly::B_QFULL), 2 * Ly::Q_BYTES);
     for (int t = 0; t < 2; ++t)
       for (int c = 0; c < Ly::KCH; ++c)
@@ -168,13 +170,18 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
   auto wwait = [&](uint32_t b, uint32_t parity, int site) {
     return __all_sync(0xFFFFFFFFu, wait(b, parity, site));
   };
+  auto commit = [&](int i) {
+    count_commit(p.bar_counts, 1u, i);
+    mma_commit(bar(i));
+  };
 #ifdef CPATTN_SERIALIZE_MMA
   // Race-detection build: every MMA group completes before the MMA warp
   // moves on (see mma_role).
   uint32_t ser_phase = 0;
   auto serialize = [&]() {
-    mma_commit(bar(Ly::B_DRAIN));
+    commit(Ly::B_DRAIN);
     mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+    count_wait(p.bar_counts, kCountRowMma, Ly::B_DRAIN);
     ser_phase ^= 1u;
   };
 #else
@@ -200,10 +207,10 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
         mma_ss(s_tmem, ad, bd, Ly::IDESC_QK, (c | kk) != 0);
       }
       serialize();
-      if (!first) mma_commit(bar(Ly::B_SLOTEMPTY + rk.slot));
+      if (!first) commit(Ly::B_SLOTEMPTY + rk.slot);
       rk.template advance<Ly::NSLOT>();
     }
-    mma_commit(bar(Ly::B_SFULL + q));
+    commit(Ly::B_SFULL + q);
     return true;
   };
   // O_q (+)= P_q V over the V tile whose first slot is at rv, P_q of global
@@ -236,7 +243,7 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
         }
       }
       serialize();
-      if (!first) mma_commit(bar(Ly::B_SLOTEMPTY + rv.slot));
+      if (!first) commit(Ly::B_SLOTEMPTY + rv.slot);
       rv.template advance<Ly::NSLOT>();
     }
     return true;
@@ -264,7 +271,7 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
     RingPos rk = rp;
     skip_slots(Ly::KCH);
     ok = issue_qk(0, rk, true) && issue_qk(1, rk, false);
-    if (ok && U.n_tiles == 1) mma_commit(bar(Ly::B_QEMPTY));
+    if (ok && U.n_tiles == 1) commit(Ly::B_QEMPTY);
     // Step v: P.V of tile v-1 and QK^T of tile v, alternating the heads.
     for (int v = 1; ok && v < U.n_tiles; ++v) {
       const RingPos rv = rp;
@@ -274,7 +281,7 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
       const uint32_t t = tile_ctr + static_cast<uint32_t>(v - 1);
       ok = issue_pv(U, 0, rv, true, v - 1, t) && issue_qk(0, rk, true) &&
            issue_pv(U, 1, rv, false, v - 1, t) && issue_qk(1, rk, false);
-      if (ok && v == U.n_tiles - 1) mma_commit(bar(Ly::B_QEMPTY));
+      if (ok && v == U.n_tiles - 1) commit(Ly::B_QEMPTY);
     }
     if (!ok) break;
     // Last step: P.V of the last tile; O_DONE[q] completes with it.
@@ -283,14 +290,15 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
     const int w = U.n_tiles - 1;
     const uint32_t t = tile_ctr + static_cast<uint32_t>(w);
     ok = issue_pv(U, 0, rv, true, w, t);
-    if (ok) mma_commit(bar(Ly::B_ODONE + 0));
+    if (ok) commit(Ly::B_ODONE + 0);
     ok = ok && issue_pv(U, 1, rv, false, w, t);
-    if (ok) mma_commit(bar(Ly::B_ODONE + 1));
+    if (ok) commit(Ly::B_ODONE + 1);
     tile_ctr += static_cast<uint32_t>(U.n_tiles);
   }
   // Every MMA issued must complete before TMEM is released.
-  mma_commit(bar(Ly::B_DRAIN));
-  mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs);
+  commit(Ly::B_DRAIN);
+  if (mbar_wait_drain(bar(Ly::B_DRAIN), ser_phase, kDrainLimitNs))
+    count_wait(p.bar_counts, kCountRowMma, Ly::B_DRAIN);
 }
 
 // ------------------------------------------------------- softmax + epilogue
@@ -419,10 +427,12 @@ __device__ __forceinline__ void softmax_role_pingpong(const PrefillParams& p, ui
       tc_fence_before();
       __syncwarp();
       if ((threadIdx.x & 31) == 0) {
-        if (drop_one)
+        if (drop_one) {
           drop_one = false;  // fault-injection hook: this arrival never happens
-        else
+        } else {
+          count_arrive(p.bar_counts, 1u, Ly::B_PFULL + q, 1);
           mbar_arrive(bar(Ly::B_PFULL + q));
+        }
       }
       ++tile_ctr;
     }
@@ -476,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const BoundedWait wait{abort_flag, p.status, p.timeout_ns};
+  const BoundedWait wait = make_wait(abort_flag, p, bar(0), warp);
 
   if (warp < kProducerWarp) {
     softmax_role_pingpong<SPLIT, VF16>(p, sbase, tmem, wait);

@@ -81,6 +81,58 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluste
 // Device status word codes (written by the first role that gives up).
 enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusLayout = 2, kStatusRange = 3 };
 
+// ------------------------------------------------------ barrier-count build
+// Built with -DCPATTN_COUNT_BARRIERS, the prefill kernels count every
+// mbarrier arrival and every completed wait into a caller-owned record per
+// CTA (kCountRecord uint32 each, indexed by blockIdx.x): row 0 holds the
+// arrivals each barrier of this CTA received (from either CTA of a pair),
+// rows 1-3 the waits completed by the softmax warps, the producer and the MMA
+// warp (one per warp and completed wait), row 4 the softmax waits for the
+// previous tile's P.V that precede a rescale of O.  A test checks at kernel
+// exit that every barrier's arrivals form whole phases and that every
+// waiter observed every phase it consumes.  In other builds these helpers
+// are empty and compile away.
+constexpr int kCountBars = 40;
+constexpr int kCountRowArrive = 0, kCountRowSoftmax = 1, kCountRowProducer = 2,
+              kCountRowMma = 3, kCountRowRescale = 4;
+constexpr int kCountRecord = 5 * kCountBars;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// n arrivals on barrier `bar` of every CTA of the cluster whose rank is set
+// in cta_mask (bit 0: rank 0; a plain launch is a cluster of one).
+__device__ __forceinline__ void count_arrive(uint32_t* counts, uint32_t cta_mask, int bar,
+                                             uint32_t n) {
+#ifdef CPATTN_COUNT_BARRIERS
+  if (counts == nullptr) return;
+  const uint32_t first = blockIdx.x - cluster_ctarank();
+  for (uint32_t r = 0; r < 2; ++r)
+    if (cta_mask & (1u << r)) atomicAdd(counts + (first + r) * kCountRecord + bar, n);
+#else
+  (void)counts, (void)cta_mask, (void)bar, (void)n;
+#endif
+}
+
+// The same for a warp-collective arrival (a tcgen05.commit that one elected
+// lane of a converged warp issues): counted once, by lane 0.
+__device__ __forceinline__ void count_commit(uint32_t* counts, uint32_t cta_mask, int bar) {
+  if ((threadIdx.x & 31) == 0) count_arrive(counts, cta_mask, bar, 1);
+}
+
+// One completed wait on barrier `bar` of this CTA, by the role of `row`.
+__device__ __forceinline__ void count_wait(uint32_t* counts, int row, int bar) {
+#ifdef CPATTN_COUNT_BARRIERS
+  if (counts != nullptr && (threadIdx.x & 31) == 0)
+    atomicAdd(counts + blockIdx.x * kCountRecord + row * kCountBars + bar, 1u);
+#else
+  (void)counts, (void)row, (void)bar;
+#endif
+}
+
 // A wait with a wall-clock limit.  On expiry it records the site in the
 // device status word, raises the CTA-wide abort flag and returns false; a
 // wait also returns false as soon as another role of the CTA has aborted,
@@ -89,14 +141,23 @@ struct BoundedWait {
   volatile int* abort_flag;  // shared memory
   int* status;               // global status word (may be null)
   uint64_t limit_ns;
+  uint32_t* counts;          // barrier-count build: the records, else unused
+  uint32_t bar0;             // shared address of barrier 0 (count index base)
+  int row;                   // count row of the waiting role
+
+  __device__ __forceinline__ BoundedWait with_row(int r) const {
+    BoundedWait w = *this;
+    w.row = r;
+    return w;
+  }
 
   __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity, int site) const {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return done(bar);
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
       for (int i = 0; i < 32; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return done(bar);
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
@@ -104,6 +165,12 @@ struct BoundedWait {
         return false;
       }
     }
+  }
+
+ private:
+  __device__ __forceinline__ bool done(uint32_t bar) const {
+    count_wait(counts, row, static_cast<int>((bar - bar0) >> 3));
+    return true;
   }
 };
 
@@ -151,18 +218,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// Same load delivered to the same shared-memory offset of every CTA in
-// cta_mask (cluster ranks); each destination CTA's mbarrier at the same
-// offset receives the transaction bytes of its copy.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                               int c0, int c1, int c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // Load for a CTA pair running 2-SM MMAs: the box lands in THIS CTA's shared
 // memory at dst, and its transaction bytes complete on the mbarrier at
 // bar_cluster -- the leader CTA's barrier (mapa_shared(bar, 0)), which is
@@ -174,12 +229,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       ".cta_group::2 [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
       : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
 }
 
 // Whole-cluster barrier (every thread of every CTA of the cluster).
@@ -299,17 +348,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "{\n\t.reg .pred e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-      : "memory");
-}
-
-// Commit that arrives on the mbarrier at the same offset in every CTA of
-// cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(bar), "h"(cta_mask)
       : "memory");
 }
 

@@ -6,8 +6,11 @@
 // HBM-bound copy.  One thread moves one 16-byte vector of K and the same
 // vector of V; consecutive threads cover consecutive vectors of one source
 // row, so loads and stores are fully coalesced within each HD*2-byte row.
-// An fp16 V cache (v_f16) receives each V value converted from bf16 (exact
-// inside fp16's range); a value outside it sets kStatusRange in *status.
+// An fp16 V cache (v_f16) receives each V value converted from bf16 with
+// round-to-nearest-even: exact for 2^-17 <= |v| <= 65504; below 2^-17 the
+// value is rounded to a multiple of 2^-24 (fp16's subnormal step), so
+// |v| <= 2^-25 becomes zero -- an absolute error of at most 2^-25, not
+// reported.  A value beyond 65504 sets kStatusRange in *status.
 #pragma once
 
 #include <cstdint>

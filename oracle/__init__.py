@@ -18,8 +18,8 @@ that the pins must catch).
 from .striped import (bf16_bits, bf16_to_f16_bits, bits_to_f64, build_striped_cache,
                       f16_bits_to_f64, read_logical, shard_fill, shard_of_token, write_kv_ref)
 from .attention import (attend_ref, attend_region_ref, attend_rows_ref, attention_probs_ref,
-                        brute_force_ref, lse_merge)
+                        brute_force_ref, kv_head_of, lse_merge)
 
 __all__ = ["bf16_bits", "bf16_to_f16_bits", "f16_bits_to_f64", "bits_to_f64", "build_striped_cache", "read_logical", "shard_fill",
            "shard_of_token", "write_kv_ref", "attend_ref", "attend_rows_ref",
-           "attend_region_ref", "attention_probs_ref", "brute_force_ref", "lse_merge"]
+           "attend_region_ref", "attention_probs_ref", "brute_force_ref", "kv_head_of", "lse_merge"]

@@ -104,8 +104,10 @@ def bf16_to_f16_bits(u16: np.ndarray) -> np.ndarray:
 
     The bf16 value (exact in float32) is rounded to the nearest binary16,
     ties to even, as IEEE 754 defines conversion to a narrower format:
-    exact for normal values within binary16's range, rounded below 2^-14
-    (subnormals), +-inf beyond 65504 + half an ulp.
+    exact for normal values within binary16's range and, since a bf16 value
+    has 8 significant bits, for subnormal results down to 2^-17; below that
+    rounded to a multiple of 2^-24 (zero at or below 2^-25); +-inf beyond
+    65504 + half an ulp.
     """
     f32 = (np.asarray(u16).astype(np.uint32) << 16).view(np.float32)
     with np.errstate(over="ignore"):

@@ -2,6 +2,8 @@
 check used by every parity test."""
 from __future__ import annotations
 
+import collections
+
 import numpy as np
 import torch
 
@@ -40,13 +42,19 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
 
 
+Parity = collections.namedtuple("Parity", "max_abs rel n_allowance max_abs_ref")
+
+
 def compare(out: np.ndarray, ref: np.ndarray, what: str = "", max_abs_bar: float = None,
-            rel_bar: float = None):
+            rel_bar: float = None) -> Parity:
     """Parity bar against the unrounded fp64 oracle: relative RMS <= 2e-3 and
     max |diff| <= 1e-2.  Where rounding the exact value to bf16 alone moves it
     by more than half that bar (|O| >= 4, half-ulp 1.6e-2), the element may
     also differ by its own rounding error plus 5e-3: no bf16 output can do
-    better there."""
+    better there.  Returns the max |diff|, the relative RMS, how many
+    elements went past the max-|diff| bar under that allowance, and
+    max |O_ref|.  Below |O_ref| = 2 the allowance never exceeds the bar (a
+    bf16 half-ulp there is at most 3.9e-3), which is asserted too."""
     assert out.shape == ref.shape, (out.shape, ref.shape)
     assert np.all(np.isfinite(out)), f"{what}: non-finite output"
     d = out - ref
@@ -57,9 +65,12 @@ def compare(out: np.ndarray, ref: np.ndarray, what: str = "", max_abs_bar: float
     excess = float(np.max(np.abs(d) - allowed))
     max_abs = float(np.max(np.abs(d)))
     rel = float(np.sqrt(np.sum(d * d) / np.sum(ref * ref)))
+    over = np.abs(d) > bar_abs
+    n_allowance = int(np.count_nonzero(over))
     assert excess <= 0 and rel <= bar_rel, \
         f"{what}: max|d|={max_abs:.3e} (<= {bar_abs} + rounding), relRMS={rel:.3e} (<= {bar_rel})"
-    return max_abs, rel
+    assert not np.any(over & (np.abs(ref) < 2)), f"{what}: allowance used where |O_ref| < 2"
+    return Parity(max_abs, rel, n_allowance, float(np.max(np.abs(ref))))
 
 
 class DeviceCase:

@@ -44,6 +44,28 @@ class Case:
                                  self.f64("k_cache"), self.f64("v_cache"), w.cache_lens,
                                  w.chunk_lens, w.chunk, w.scale, threads=threads)
 
+    def oracle_heads(self, heads):
+        """The oracle's whole output for the listed q heads only: O [T,
+        len(heads), HD] and LSE [T, len(heads)] (NaN pad rows), one q head at
+        a time against its own kv head's keys, the heads run in parallel."""
+        from concurrent.futures import ThreadPoolExecutor
+        w = self.w
+        G = w.num_q_heads // w.num_kv_heads
+        vconv = oracle.f16_bits_to_f64 if self.v_f16 else oracle.bits_to_f64
+
+        def one(h):
+            g = oracle.kv_head_of(h, G)
+            return oracle.attend_ref(
+                oracle.bits_to_f64(self.q_bits[:, [h]]), oracle.bits_to_f64(self.k_new_bits[:, [g]]),
+                oracle.bits_to_f64(self.v_new_bits[:, [g]]),
+                oracle.bits_to_f64(self.k_cache_bits[:, [g]]), vconv(self.v_cache_bits[:, [g]]),
+                w.cache_lens, w.chunk_lens, w.chunk, w.scale)
+
+        with ThreadPoolExecutor(min(len(heads), os.cpu_count() or 1)) as ex:
+            res = list(ex.map(one, heads))
+        return (np.concatenate([o for o, _ in res], axis=1),
+                np.concatenate([l for _, l in res], axis=1))
+
     def oracle_rows(self, samples):
         w = self.w
         vc = self.f64("v_cache") if self.v_f16 else self.v_cache_bits
@@ -65,6 +87,25 @@ def make_case(w: Workload, hole_bits=POISON_BITS, v_f16: bool = False) -> Case:
     return Case(w=w, inputs=inp, q_bits=oracle.bf16_bits(inp.q),
                 k_new_bits=oracle.bf16_bits(inp.k_new), v_new_bits=oracle.bf16_bits(inp.v_new),
                 k_cache_bits=kc, v_cache_bits=vc, v_f16=v_f16)
+
+
+def heads_per_kv_head(w: Workload, pairs: bool = True, seed: int = 99):
+    """Seeded q heads to compare whole: for every kv head g, a pair of
+    adjacent heads (2j, 2j + 1) of its group -- the two heads one CTA pair
+    computes together -- or, pairs=False, one head (even for even g, odd for
+    odd g, so both CTAs of a pair are covered across kv heads)."""
+    rng = np.random.default_rng(seed)
+    G = w.num_q_heads // w.num_kv_heads
+    heads = []
+    for g in range(w.num_kv_heads):
+        j = int(rng.integers(max(G // 2, 1)))
+        if G == 1:
+            heads.append(g)
+        elif pairs:
+            heads += [g * G + 2 * j, g * G + 2 * j + 1]
+        else:
+            heads.append(g * G + 2 * j + (g & 1))
+    return heads
 
 
 def sample_rows(w: Workload, n: int, seed: int = 1234):

@@ -65,12 +65,50 @@ def test_create_rejects(lib, cfg, status):
     assert e.value.status == status
 
 
-@pytest.mark.parametrize("value,ok", [("mma2", True), ("multicast", True), ("none", True),
-                                      ("pingpong", True),
-                                      ("both", False), ("", False)])
-def test_pairing_mode_from_environment(lib, monkeypatch, value, ok):
-    """CPATTN_PAIRING is read at create; an unknown value is rejected there
-    rather than silently running another kernel."""
+@pytest.mark.parametrize("field,value", [("fast_p", 2), ("v_cache_f16", -1), ("pairing", 3),
+                                         ("pairing", -1), ("gqa_packing", 2)])
+def test_create_rejects_config_fields(lib, field, value):
+    """Every enumerated field of cpattn_config is range-checked at create, and
+    by the allocation-free prefill before anything runs."""
+    cfg = cp.binding.Config(8, 2, 128, 2, 64, 32, 0.0, 0, 0, 0, 0)
+    setattr(cfg, field, value)
+    h = ctypes.c_void_p()
+    assert lib.cpattn_create(ctypes.byref(cfg), ctypes.byref(h)) == cp.E_INVALID
+    assert not h.value
+    A = 256
+    assert cp.binding.prefill_noalloc(cfg, [0], [1], A, A, A, A, A, A, stream=0) == cp.E_INVALID
+
+
+def test_too_many_q_heads_unsupported(lib):
+    """More than 65535 q heads would overflow the kernel's unit count: refused
+    by create and by the allocation-free prefill alike."""
+    cfg = cp.binding.Config(65536, 1, 128, 2, 64, 32, 0.0, 0, 0, 0, 0)
+    h = ctypes.c_void_p()
+    assert lib.cpattn_create(ctypes.byref(cfg), ctypes.byref(h)) == cp.E_UNSUPPORTED
+    A = 256
+    assert cp.binding.prefill_noalloc(cfg, [0], [1], A, A, A, A, A, A,
+                                      stream=0) == cp.E_UNSUPPORTED
+
+
+def test_pairing_and_packing_from_config(lib):
+    """The kernel form is a configuration field: pairing "pingpong" plans one
+    executor per SM at HD = 128 (more split pieces than 2-SM pairs), and
+    gqa_packing off leaves a decode step unpacked."""
+    a = cp.Context(8, 2, 128, 8, 8000, 128, pairing="mma2")
+    b = cp.Context(8, 2, 128, 8, 8000, 128, pairing="pingpong")
+    assert b.splitkv_workspace([60000], [100], 0)[1] > a.splitkv_workspace([60000], [100], 0)[1]
+    on = cp.Context(32, 2, 256, 8, 1000, 64)
+    off = cp.Context(32, 2, 256, 8, 1000, 64, gqa_packing=False)
+    assert on.splitkv_workspace([5000, 5000], [64, 1], 1 << 20)[1] == 8 + 1
+    assert off.splitkv_workspace([5000, 5000], [64, 1], 1 << 20)[1] == 2
+
+
+@pytest.mark.parametrize("value,ok", [("mma2", True), ("none", True), ("pingpong", True),
+                                      ("multicast", False), ("both", False), ("", False)])
+def test_pairing_override_from_environment(lib, monkeypatch, value, ok):
+    """CPATTN_PAIRING (a test override of cpattn_config.pairing) is read at
+    create; an unknown value is rejected there rather than silently running
+    another kernel."""
     monkeypatch.setenv("CPATTN_PAIRING", value)
     if ok:
         cp.Context(8, 2, 128, 2, 64, 32).close()
@@ -81,10 +119,11 @@ def test_pairing_mode_from_environment(lib, monkeypatch, value, ok):
 
 
 @pytest.mark.parametrize("value,ok", [("auto", True), ("off", True), ("on", False)])
-def test_gqa_packing_from_environment(lib, monkeypatch, value, ok):
+def test_gqa_packing_override_from_environment(lib, monkeypatch, value, ok):
     monkeypatch.setenv("CPATTN_GQA_PACKING", value)
     if ok:
-        ctx = cp.Context(32, 2, 256, 8, 1000, 64)
+        # The override wins over the configuration field.
+        ctx = cp.Context(32, 2, 256, 8, 1000, 64, gqa_packing=(value == "off"))
         # A decode step is packed (one 8-token block) unless packing is off.
         _, blocks = ctx.splitkv_workspace([5000], [1], 1 << 20)
         assert blocks == 1
@@ -94,6 +133,24 @@ def test_gqa_packing_from_environment(lib, monkeypatch, value, ok):
         with pytest.raises(cp.CpattnError) as e:
             cp.Context(32, 2, 256, 8, 1000, 64)
         assert e.value.status == cp.E_INVALID
+
+
+def test_no_multicast_tma_load_in_the_sources():
+    """The library may be launched on several GPUs (one replica per GPU), so
+    no TMA load in it may use cluster multicast; mbarrier signals
+    (tcgen05.commit ... multicast::cluster) are not loads and are allowed."""
+    d = os.path.join(ROOT, "long_context_chunked_gb300", "csrc")
+    for name in sorted(os.listdir(d)) + ["../../include/cpattn.h"]:
+        text = open(os.path.join(d, name)).read()
+        assert not re.search(r"cp\.async\.bulk[^;]*multicast", text), name
+
+
+def test_barrier_counts_need_the_count_build(lib):
+    """The release library refuses barrier counting; the count build accepts
+    a record buffer and rejects a misaligned one."""
+    ctx = cp.Context(8, 2, 128, 2, 64, 32)
+    assert ctx.lib.cpattn_set_barrier_counts(ctx._h, 4096, 4096) == cp.E_UNSUPPORTED
+    assert ctx.lib.cpattn_set_barrier_counts(ctx._h, None, 0) == cp.E_UNSUPPORTED
 
 
 def test_prefill_and_write_validation(lib):
@@ -228,16 +285,15 @@ def test_splitkv_workspace_too_small_is_refused_before_launch(lib):
     assert st == cp.E_INVALID and "split-KV workspace" in ctx.last_error()
 
 
-def test_pingpong_plans_per_sm(lib, monkeypatch):
+def test_pingpong_plans_per_sm(lib):
     """Two query tiles per CTA: every SM is an executor of head pairs, so a
     short chunk against a long cache is cut into more pieces than for CTA
     pairs (one executor per two SMs); at HD = 256 the mode runs as 2-SM
     pairs and plans exactly like them."""
     plans = {}
     for mode in ("mma2", "pingpong"):
-        monkeypatch.setenv("CPATTN_PAIRING", mode)
         for hd in (128, 256):
-            ctx = cp.Context(8, 2, hd, 8, 8000, 128)
+            ctx = cp.Context(8, 2, hd, 8, 8000, 128, pairing=mode)
             plans[mode, hd] = ctx.splitkv_workspace([60000], [100], 0)
             ctx.close()
     assert plans["pingpong", 256] == plans["mma2", 256]

@@ -1,12 +1,11 @@
 """The head pairing modes of the fused prefill against the fp64 oracle.
 
 With an even group size the library pairs adjacent q heads of one kv head.
-CPATTN_PAIRING (read when a context is created) picks how: 'mma2' -- the
-leader CTA of a CTA pair issues 2-SM MMAs (M = 256) and each CTA stages half
-of every K/V tile; 'multicast' -- each CTA issues its own MMAs and the pair
-shares K/V loads by multicast; 'pingpong' -- one CTA holds both heads' query
-tiles and alternates their products (HD = 128; 'mma2' at HD = 256);
-'none' -- one CTA per unit.  Every mode must
+cpattn_config.pairing picks how: 'mma2' -- the leader CTA of a CTA pair
+issues 2-SM MMAs (M = 256) and each CTA stages half of every K/V tile;
+'pingpong' -- one CTA holds both heads' query tiles and alternates their
+products (HD = 128; 'mma2' at HD = 256); 'none' -- one CTA per unit.  Every
+mode must
 meet the same bar on cases with several tiles, ragged chunks and an empty
 cache, in both P precisions."""
 import numpy as np
@@ -19,7 +18,7 @@ from workloads import small
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["mma2", "multicast", "none", "pingpong"]
+MODES = ["mma2", "none", "pingpong"]
 CASES = [
     small("pairA", (0, 1000, 129), (300, 130, 256), 320, nq=8, nkv=2, hd=128, shards=4,
           shard_capacity=300, seed=41),
@@ -32,11 +31,10 @@ CASES = [
 @pytest.mark.parametrize("fast_p", [False, True], ids=["accurate", "fast_p"])
 @pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
 @pytest.mark.parametrize("mode", MODES)
-def test_pairing_mode_parity(mode, w, fast_p, monkeypatch):
-    monkeypatch.setenv("CPATTN_PAIRING", mode)
+def test_pairing_mode_parity(mode, w, fast_p):
     case = make_case(w)
     dc = DeviceCase(case)
-    ctx = cp.Context.for_workload(w, fast_p=fast_p)
+    ctx = cp.Context.for_workload(w, fast_p=fast_p, pairing=mode)
     dc.prefill(ctx)
     ref, ref_lse = case.oracle_full()
     v = dc.valid_rows()
@@ -55,15 +53,14 @@ def test_pairing_mode_parity(mode, w, fast_p, monkeypatch):
     assert dc.guards_intact(), "write outside a buffer"
 
 
-def test_pairing_modes_repeatable(monkeypatch):
+def test_pairing_modes_repeatable():
     """Each mode gives identical bits on a second launch (a race in the
     pair's cross-CTA barriers would show up as run-to-run differences)."""
     w = CASES[2]
     case = make_case(w)
     dc = DeviceCase(case)
     for mode in MODES:
-        monkeypatch.setenv("CPATTN_PAIRING", mode)
-        ctx = cp.Context.for_workload(w)
+        ctx = cp.Context.for_workload(w, pairing=mode)
         dc.prefill(ctx)
         first = dc.out.bits().copy()
         for _ in range(3):

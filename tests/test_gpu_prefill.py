@@ -1,9 +1,11 @@
 """Fused prefill on the GPU against the fp64 oracle.
 
 Small cases compare every valid output element; the four full-size
-workloads compare seeded sampled rows (first/last rows of each sequence and
-q block edges included) plus whole-output properties, in the launch
-configuration the benchmark uses.  Bar: max |diff| <= 1e-2 and relative RMS
+workloads, in the launch configuration the benchmark uses, compare every
+valid row of whole q heads (an adjacent pair per kv head -- the two heads
+one CTA pair computes -- at 8k, 32k and varlen, one head per kv head at
+128k), seeded sampled rows of all heads (first/last rows of each sequence
+and q block edges included), and whole-output properties.  Bar: max |diff| <= 1e-2 and relative RMS
 <= 2e-3.  Cache holes hold large finite poison; guard bands around every
 buffer must survive."""
 import numpy as np
@@ -13,7 +15,7 @@ import torch
 import oracle
 import long_context_chunked_gb300 as cp
 from gpu_helpers import DeviceCase, compare, to_f64
-from helpers import POISON_BITS, make_case, sample_rows
+from helpers import POISON_BITS, heads_per_kv_head, make_case, sample_rows
 from workloads import ALL, CTX_8K, CTX_32K, CTX_128K, TINY, VARLEN, small
 
 pytestmark = pytest.mark.gpu
@@ -79,19 +81,28 @@ def full_runs():
 
 
 @pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
-def test_full_size_sampled(w, full_runs):
+def test_full_size(w, full_runs):
     case = make_case(w)
     dc = DeviceCase(case)
     ctx = cp.Context.for_workload(w)
     dc.prefill(ctx)
+    out = to_f64(dc.out.bits())
+    v = dc.valid_rows()
+    # Whole q heads: every valid row of every sequence.
+    heads = heads_per_kv_head(w, pairs=w is not CTX_128K)
+    href, href_lse = case.oracle_heads(heads)
+    whole = compare(out[v][:, heads], href[v], f"{w.name} heads {heads}")
+    if whole.max_abs_ref < 2:
+        assert whole.n_allowance == 0
+    lse_all = dc.lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse_all[v][:, heads] - href_lse[v])) < 2e-3, "LSE (whole heads)"
+    # Sampled rows of every head.
     samples = sample_rows(w, 48, seed=w.seed)
     ref, ref_lse = case.oracle_rows(samples)
-    out = to_f64(dc.out.bits())
     got = np.stack([out[t, h] for t, h in samples])
-    max_abs, rel = compare(got, ref, w.name)
+    max_abs, rel = compare(got, ref, w.name)[:2]
     lse = dc.lse.cpu().numpy()
     assert np.max(np.abs(np.array([lse[t, h] for t, h in samples]) - ref_lse)) < 2e-3
-    v = dc.valid_rows()
     assert np.all(np.isfinite(out[v])), "non-finite output"
     assert np.all(np.abs(out[v]) < 16), "output outside the convex hull of V"
     assert dc.guards_intact()

@@ -64,7 +64,7 @@ def test_prefill_write_kv(w):
     _run(w)
 
 
-@pytest.mark.parametrize("mode", ["none", "multicast", "pingpong"])
+@pytest.mark.parametrize("mode", ["none", "pingpong"])
 def test_prefill_write_kv_pairing_modes(mode, monkeypatch):
     monkeypatch.setenv("CPATTN_PAIRING", mode)
     _run(CASES[0])

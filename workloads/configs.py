@@ -147,3 +147,46 @@ def small(name: str, cache_lens, chunk_lens, chunk, nq=4, nkv=2, hd=128, shards=
     return Workload(name=name, cache_lens=cache_lens, chunk_lens=chunk_lens, chunk=chunk,
                     num_q_heads=nq, num_kv_heads=nkv, head_dim=hd, shards=shards,
                     shard_capacity=shard_capacity, seed=seed, peaky_frac=peaky_frac)
+
+
+@dataclasses.dataclass(frozen=True)
+class Request:
+    """A whole chunked prefill of one batch of requests: step k brings
+    ``steps[k][b]`` new tokens of sequence b (0..chunk), and its cache then
+    holds every token of the earlier steps -- the PR's per-request cumulative
+    prefill (Performance section), with the KV write of each chunk between
+    the steps."""
+    name: str
+    steps: Tuple[Tuple[int, ...], ...]
+    chunk: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    shards: int
+    shard_capacity: int
+    seed: int
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.steps[0])
+
+    def step(self, k: int) -> Workload:
+        """Step k as a one-step workload (sizes only; its inputs come from
+        ``generate_request``)."""
+        cache = tuple(sum(s[b] for s in self.steps[:k]) for b in range(self.num_seqs))
+        return Workload(name=f"{self.name}/{k}", cache_lens=cache, chunk_lens=self.steps[k],
+                        chunk=self.chunk, num_q_heads=self.num_q_heads,
+                        num_kv_heads=self.num_kv_heads, head_dim=self.head_dim,
+                        shards=self.shards, shard_capacity=self.shard_capacity, seed=self.seed)
+
+
+def request(name: str, steps, chunk, nq=4, nkv=2, hd=128, shards=3, seed=300,
+            shard_capacity=None) -> Request:
+    """A small cumulative request; the shard capacity defaults to the least
+    that holds every sequence's whole request."""
+    steps = tuple(tuple(int(x) for x in s) for s in steps)
+    total = max(sum(s[b] for s in steps) for b in range(len(steps[0])))
+    if shard_capacity is None:
+        shard_capacity = max(1, -(-total // shards))
+    return Request(name=name, steps=steps, chunk=chunk, num_q_heads=nq, num_kv_heads=nkv,
+                   head_dim=hd, shards=shards, shard_capacity=shard_capacity, seed=seed)

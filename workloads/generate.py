@@ -14,7 +14,7 @@ from typing import List
 
 import torch
 
-from .configs import Workload
+from .configs import Request, Workload
 
 
 @dataclasses.dataclass
@@ -59,3 +59,24 @@ def generate(w: Workload, seed: int | None = None) -> Inputs:
             k_new[in_chunk] = k_new[in_chunk] * 2
     return Inputs(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
                   peaky_positions=peaky)
+
+
+@dataclasses.dataclass
+class StepInputs:
+    q: torch.Tensor       # [B*C, NQ, HD] bf16, token order, pad rows included
+    k_new: torch.Tensor   # [B*C, NKV, HD] bf16
+    v_new: torch.Tensor   # [B*C, NKV, HD] bf16
+
+
+def generate_request(r: Request) -> List[StepInputs]:
+    """Every step's chunk of a cumulative request, from one generator in step
+    order: Q, then K_new, then V_new of each step (N(0, 1), bf16)."""
+    gen = torch.Generator().manual_seed(r.seed)
+    T = r.num_seqs * r.chunk
+    out = []
+    for _ in r.steps:
+        q = _normal_bf16(gen, T, r.num_q_heads, r.head_dim)
+        k = _normal_bf16(gen, T, r.num_kv_heads, r.head_dim)
+        v = _normal_bf16(gen, T, r.num_kv_heads, r.head_dim)
+        out.append(StepInputs(q=q, k_new=k, v_new=v))
+    return out
