@@ -62,16 +62,14 @@ def csrc_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def prefill_kernel_name(w) -> str:
+def prefill_kernel_name(w, pairing: str = "mma2") -> str:
     """The prefill kernel the library launches for this workload: paired heads
-    (CPATTN_PAIRING, default 2-SM MMA) when the group size is even."""
-    mode = os.environ.get("CPATTN_PAIRING", "mma2") if w.group % 2 == 0 else "none"
+    (cpattn_config.pairing, default 2-SM MMA) when the group size is even."""
+    mode = os.environ.get("CPATTN_PAIRING", pairing) if w.group % 2 == 0 else "none"
     if mode == "pingpong" and w.head_dim == 128:
         return "prefill_kernel_pingpong<128>"
     if mode in ("mma2", "pingpong"):
         return "prefill_kernel_pair2<%d>" % w.head_dim
-    if mode == "multicast":
-        return "prefill_kernel<%d> (multicast pairs)" % w.head_dim
     return "prefill_kernel<%d>" % w.head_dim
 
 
@@ -153,14 +151,14 @@ class DeviceState:
     library's own KV write."""
 
     def __init__(self, w: Workload, device, fast_p: bool = False, variant: str = "fused",
-                 v_f16: bool = False):
+                 v_f16: bool = False, pairing: str = "mma2"):
         import torch
         import long_context_chunked_gb300 as cp
         self.w = w
         self.variant = variant
         inp = generate(w)
         self.inp = inp
-        self.ctx = cp.Context.for_workload(w, fast_p=fast_p, v_cache_f16=v_f16)
+        self.ctx = cp.Context.for_workload(w, fast_p=fast_p, v_cache_f16=v_f16, pairing=pairing)
         self.q = inp.q.to(device)
         self.k_new = inp.k_new.to(device)
         self.v_new = inp.v_new.to(device)
@@ -239,6 +237,79 @@ def time_steps(st: DeviceState, steps: int, warmup: int, flush):
     if st.ctx.sync_status() != 0:
         raise RuntimeError("device status after timing: " + st.ctx.last_error())
     return step_ms, prefill_ms
+
+
+def max_abs_valid(st: DeviceState) -> float:
+    """max |O| over the valid output rows of the last step (it bounds the
+    oracle's max |O_ref| within the parity bar; the parity tests report
+    max |O_ref| itself)."""
+    w = st.w
+    rows = [st.out[b * w.chunk: b * w.chunk + c] for b, c in enumerate(w.chunk_lens) if c]
+    return max(float(r.abs().max().item()) for r in rows)
+
+
+def measure_config(w: Workload, device, flush, steps: int, warmup: int, v_f16: bool,
+                   peak: float, fast_p: bool = False) -> dict:
+    """One workload's step (write_kv + prefill), timed as the headline is:
+    L2 flushed between steps, CUDA events on the launching stream, SM clocks
+    sampled during the timed region."""
+    import torch
+    st = DeviceState(w, device, fast_p=fast_p, v_f16=v_f16)
+    torch.cuda.synchronize()
+    with ClockSampler(device.index or 0) as clk:
+        step_ms, prefill_ms = time_steps(st, steps, warmup, flush)
+    flops = w.attention_flops()
+    pf, ms = statistics.mean(prefill_ms), statistics.mean(step_ms)
+    rec = {"workload": w.name, "description": w.description, "steps": steps,
+           "v_cache": "f16" if v_f16 else "bf16", "precision": precision_label(fast_p, v_f16),
+           "ms": round(ms, 4), "prefill_ms": round(pf, 4),
+           "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+           "prefill_tflops": round(flops / (pf * 1e-3) / 1e12, 2),
+           "frac": round(flops / (pf * 1e-3) / 1e12 / peak, 4),
+           "kernel": prefill_kernel_name(w), "max_abs_out": round(max_abs_valid(st), 4),
+           "clocks": clk.summary()}
+    del st
+    torch.cuda.empty_cache()
+    return rec
+
+
+def same_run_peaks(device) -> dict:
+    """The roofline denominators re-measured in this run, on this GPU: a bf16
+    8192^3 torch.matmul (cuBLAS; best of 10, CUDA events) and a 2 GiB device
+    copy (read + write bytes, best of 10), with SM clocks sampled meanwhile."""
+    import torch
+    n = 8192
+    a = torch.randn(n, n, device=device, dtype=torch.bfloat16)
+    b = torch.randn(n, n, device=device, dtype=torch.bfloat16)
+    src = torch.empty(1 << 30, dtype=torch.bfloat16, device=device).fill_(1.0)
+    dst = torch.empty_like(src)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index or 0) as clk:
+        for _ in range(3):
+            a @ b
+        mm = []
+        for _ in range(10):
+            e0, e1 = ev(), ev()
+            e0.record()
+            a @ b
+            e1.record()
+            torch.cuda.synchronize()
+            mm.append(e0.elapsed_time(e1))
+        cp_ms = []
+        for _ in range(10):
+            e0, e1 = ev(), ev()
+            e0.record()
+            dst.copy_(src)
+            e1.record()
+            torch.cuda.synchronize()
+            cp_ms.append(e0.elapsed_time(e1))
+    res = {"bf16_tflops": round(2 * n ** 3 / (min(mm) * 1e-3) / 1e12, 1),
+           "hbm_gbs": round(2 * src.numel() * 2 / (min(cp_ms) * 1e-3) / 1e9, 1),
+           "how": "torch.matmul bf16 8192^3 and a 2 GiB copy_, best of 10 each, in this run",
+           "clocks": clk.summary()}
+    del a, b, src, dst
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_e2e(st: DeviceState, steps: int, warmup: int, slots: int = 2):
@@ -341,7 +412,8 @@ def cpu_sample(w: Workload, budget_rows: int = 384, heads: int = 2):
     dt = time.perf_counter() - t0
     flops = 4 * hd * heads * (rows * L + rows * (rows + 1) // 2)
     desc = (f"{w.name}: sequence 0, {heads} q heads of kv head 0, chunk rows 0..{rows - 1}, "
-            f"full cache of {L} tokens ({flops / 1e9:.1f} GFLOP), {threads} worker threads")
+            f"full cache of {L} tokens ({flops / 1e9:.1f} GFLOP), {threads} worker threads "
+            f"(one per q head) on a host of {os.cpu_count()} cores")
     return flops / dt / 1e12, dt, desc, threads
 
 
@@ -369,15 +441,18 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     w = BY_NAME[args.config]
+    # One worker thread per q head, as many heads of kv head 0 as the host
+    # has cores (the oracle's BLAS calls may use more threads inside).
+    heads = max(1, min(os.cpu_count() or 1, w.group))
     vals = []
     for _ in range(args.warmup):
-        cpu_sample(w, budget_rows=args.ref_rows)
+        cpu_sample(w, budget_rows=args.ref_rows, heads=heads)
     for _ in range(args.steps):
-        tf, dt, desc, threads = cpu_sample(w, budget_rows=args.ref_rows)
+        tf, dt, desc, threads = cpu_sample(w, budget_rows=args.ref_rows, heads=heads)
         vals.append((tf, dt))
     v = statistics.median(t for t, _ in vals)
     sec = statistics.median(d for _, d in vals)
-    cores = threads
+    cores = os.cpu_count()
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -385,7 +460,7 @@ def run_reference(args, world, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16 inputs)",
         "config": {"workload": w.name, "description": w.description},
         "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores,
-                         "kind": "oracle", "sample": desc},
+                         "threads": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -400,10 +475,11 @@ PAGES_TTFT_MS = {8192: 2.55, 16384: 6.29, 32768: 17.23, 65536: 53.05, 131072: 18
                  262144: 661.0, 1048576: 9769.0}
 
 
-def run_cumulative(contexts, fast_p=False, seed=7, v_f16=False):
+def run_cumulative(contexts, fast_p=False, seed=7, v_f16=False, emit=True):
     """Every 4096-token chunk of one request of each context length, back to
     back on one stream: write the chunk into the striped cache, then prefill it
-    against everything before it.  Prints one JSON line per context."""
+    against everything before it.  Returns one record per context (and prints
+    each as a JSON line when emit)."""
     import torch
     import long_context_chunked_gb300 as cp
     dev = torch.device("cuda", 0)
@@ -413,6 +489,7 @@ def run_cumulative(contexts, fast_p=False, seed=7, v_f16=False):
     kn = torch.randn(C, NKV, HD, generator=gen).to(torch.bfloat16).to(dev)
     vn = torch.randn(C, NKV, HD, generator=gen).to(torch.bfloat16).to(dev)
     out = torch.empty_like(q)
+    records = []
     for n in contexts:
         S = (n + P - 1) // P
         kc = torch.zeros((1, NKV, P, S, HD), dtype=torch.bfloat16, device=dev)
@@ -436,12 +513,16 @@ def run_cumulative(contexts, fast_p=False, seed=7, v_f16=False):
             raise RuntimeError(ctx.last_error())
         ms = e0.elapsed_time(e1)
         flops = sum(4 * HD * NQ * (C * k * C + C * (C + 1) // 2) for k in range(chunks))
-        print(json.dumps({"mode": "cumulative_prefill", "context": n, "chunks": chunks,
-                          "request_ms": round(ms, 3), "tflops": round(flops / ms / 1e9, 1),
-                          "precision": precision_label(fast_p, v_f16),
-                          "v_cache": "f16" if v_f16 else "bf16",
-                          "pages_tpu_v7x8_fused_ring_ms": PAGES_TTFT_MS.get(n)}), flush=True)
+        rec = {"mode": "cumulative_prefill", "context": n, "chunks": chunks,
+               "request_ms": round(ms, 3), "tflops": round(flops / ms / 1e9, 1),
+               "precision": precision_label(fast_p, v_f16),
+               "v_cache": "f16" if v_f16 else "bf16",
+               "pages_tpu_v7x8_fused_ring_ms": PAGES_TTFT_MS.get(n)}
+        records.append(rec)
+        if emit:
+            print(json.dumps(rec), flush=True)
         del kc, vc, ctx
+    return records
 
 
 # Small-chunk and decode workloads for split-KV (NQ=32, NKV=2, HD=256, P=8,
@@ -589,6 +670,9 @@ def main():
     ap.add_argument("--cumulative", default=None,
                     help="comma-separated request lengths (e.g. 8k,32k,1M): per-request "
                          "cumulative prefill instead of the step benchmark")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the headline workload: skip the other configs, the bf16 V "
+                         "cache record, the cumulative requests and the same-run peaks")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.splitkv:
@@ -667,13 +751,36 @@ def main():
         "gpu_launches": {"fused": 2, "two_launch": 4, "fused_write": 1}[args.variant] * args.steps,
         "clocks": clk.summary(),
     }
+    if not args.no_extras and world == 1:
+        # Beside the headline, every other configuration and the bf16 V cache
+        # (every tile takes the bf16 hi+lo P pair, and the KV write is a pure
+        # bit copy), each timed as the headline is; then whole cumulative
+        # requests, and the roofline denominators re-measured in this run.
+        extra_steps = max(5, min(args.steps, 20))
+        per = {}
+        for name in ("tiny", "8k", "128k", "varlen"):
+            if name != w.name:
+                per[name] = measure_config(BY_NAME[name], device, flush, extra_steps, 3,
+                                           v_f16, peak, args.fast_p)
+        line["per_config"] = per
+        line["max_abs_out"] = round(max_abs_valid(st), 4)
+        del st
+        torch.cuda.empty_cache()
+        line["bf16_v_cache"] = measure_config(w, device, flush, extra_steps, 3, False, peak,
+                                              args.fast_p)
+        line["cumulative"] = run_cumulative([8192, 32768, 131072], fast_p=args.fast_p,
+                                            v_f16=v_f16, emit=False)
+        sr = same_run_peaks(device)
+        line["roofline"]["peak_same_run"] = sr["bf16_tflops"]
+        line["roofline"]["frac_of_same_run"] = round(achieved / sr["bf16_tflops"], 4)
+        line["same_run_peaks"] = sr
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # About 10 s of oracle work on a 16-core host: up to 16 q heads of kv
         # head 0 (one worker thread each) and up to 2048 chunk rows.
         tf, dt, desc, threads = cpu_sample(w, budget_rows=2048, heads=min(16, w.group))
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s",
-                                "cores": threads, "kind": "oracle", "sample": desc,
-                                "seconds": round(dt, 2)}
+                                "cores": os.cpu_count(), "threads": threads, "kind": "oracle",
+                                "sample": desc, "seconds": round(dt, 2)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
