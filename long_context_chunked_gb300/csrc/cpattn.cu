@@ -48,6 +48,10 @@ struct cpattn_ctx {
   // GQA packing for short-chunk launches (cpattn_config.gqa_packing, or the
   // CPATTN_GQA_PACKING override).
   bool gqa_packing = true;
+  std::vector<int> block_lens;  // scratch of the unit-order choice
+  // Unit order (test override CPATTN_UNIT_ORDER): 0 chosen by the cost
+  // model, 1 longest first, 2 kv-head-major.
+  int unit_order = 0;
   // Barrier-count build: caller-owned per-CTA count records, and their bytes.
   uint32_t* bar_counts = nullptr;
   size_t bar_counts_bytes = 0;
@@ -403,6 +407,16 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
     prm.part[i] = w.part;
   }
   prm.num_units = static_cast<int>(plan.blocks.size()) * (packed ? NKV : NQ);
+  prm.num_blocks = static_cast<int>(plan.blocks.size());
+  if (!packed) {
+    std::vector<int>& lens = ctx->block_lens;
+    lens.clear();
+    for (const cpattn::WorkBlock& b : plan.blocks) lens.push_back(b.v1 - b.v0);
+    // Executors take units_per_block units of a block (q heads, or head pairs).
+    prm.kv_major = ctx->unit_order == 2 ||
+                   (ctx->unit_order == 0 &&
+                    cpattn::prefer_kv_major(lens, units_per_block / NKV, NKV, executors));
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cpattn_status s = dispatch_prefill(ctx, &prm, st, packed);
@@ -466,6 +480,16 @@ cpattn_status cpattn_create(const cpattn_config* cfg, cpattn_ctx** out) {
   if (packing != nullptr) {
     if (std::strcmp(packing, "off") == 0) ctx->gqa_packing = false;
     else if (std::strcmp(packing, "auto") == 0) ctx->gqa_packing = true;
+    else {
+      delete ctx;
+      return CPATTN_E_INVALID;
+    }
+  }
+  const char* order = std::getenv("CPATTN_UNIT_ORDER");
+  if (order != nullptr) {
+    if (std::strcmp(order, "auto") == 0) ctx->unit_order = 0;
+    else if (std::strcmp(order, "longest") == 0) ctx->unit_order = 1;
+    else if (std::strcmp(order, "kv_major") == 0) ctx->unit_order = 2;
     else {
       delete ctx;
       return CPATTN_E_INVALID;

@@ -59,6 +59,41 @@ inline long long cyclic_makespan(const std::vector<int>& lens, int units_per_blo
 }
 constexpr int kMaxVirtualTiles = 65535;  // v0 and v1 are packed in 16 bits each
 
+// Makespan of units dealt to E executors in snake order (executor e takes
+// slot e of even rounds, slot E-1-e of odd ones), each costing its tiles plus
+// the fill/drain overhead; lens[u] is unit u's tiles, in unit-index order.
+inline long long snake_makespan(const std::vector<int>& lens, int executors) {
+  const int E = std::max(executors, 1);
+  std::vector<long long> load(static_cast<size_t>(E), 0);
+  for (size_t u = 0; u < lens.size(); ++u) {
+    const long long r = static_cast<long long>(u) / E;
+    const int slot = static_cast<int>(u % E);
+    load[static_cast<size_t>((r & 1) ? E - 1 - slot : slot)] += lens[u] + kUnitOverheadTiles;
+  }
+  return *std::max_element(load.begin(), load.end());
+}
+
+// Whether to deal units kv-head-major (see PrefillParams::kv_major): units
+// that run at once then read one kv head's K/V, so it is fetched from DRAM
+// about once instead of once per round of the grid.  Taken when it costs the
+// grid at most 1 % of the longest-first order's makespan (the measure of a
+// compute-bound launch); block_lens: the work blocks' tiles, longest first;
+// per_kv: units of one kv head per block.
+inline bool prefer_kv_major(const std::vector<int>& block_lens, int per_kv, int nkv,
+                            int executors) {
+  const size_t units = block_lens.size() * static_cast<size_t>(per_kv) * nkv;
+  if (nkv < 2 || units <= static_cast<size_t>(executors)) return false;
+  std::vector<int> lf, kv;
+  lf.reserve(units);
+  kv.reserve(units);
+  for (int len : block_lens)
+    for (int j = 0; j < per_kv * nkv; ++j) lf.push_back(len);
+  for (int g = 0; g < nkv; ++g)
+    for (int len : block_lens)
+      for (int j = 0; j < per_kv; ++j) kv.push_back(len);
+  return snake_makespan(kv, executors) * 100 <= snake_makespan(lf, executors) * 101;
+}
+
 struct WorkBlock {
   int b, qb, v0, v1;
   int part;  // -1: writes the output; else the first partial row of a piece

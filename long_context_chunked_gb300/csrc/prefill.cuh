@@ -64,6 +64,11 @@ struct PrefillParams {
   int* status;
   unsigned long long timeout_ns;
   int num_units, nq, nkv, group, P, S, C, debug_flags;
+  // Unit order: 0 -- unit u is q head (or packed kv head) u % per of work
+  // block u / per, blocks longest first; 1 (kv-head-major) -- all units of
+  // kv head 0 (every block, longest first), then kv head 1, ...: the units
+  // that run together read one kv head's K/V, which then stays in L2.
+  int kv_major, num_blocks;
   // out_f32: O is written to `out` as fp32 (the two-launch variant's partial
   // results) instead of bf16.
   int out_f32;
@@ -164,8 +169,18 @@ struct Unit {
 __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
   Unit U;
   const int per = p.packed ? p.nkv : p.nq;  // units per work block
-  const int blk = u / per;
-  const int k = u - blk * per;
+  int blk, k;
+  if (p.kv_major) {
+    const int gu = per / p.nkv;               // units of one kv head per block
+    const int span = p.num_blocks * gu;       // units of one kv head
+    const int g = u / span;
+    const int rem = u - g * span;
+    blk = rem / gu;
+    k = g * gu + (rem - blk * gu);
+  } else {
+    blk = u / per;
+    k = u - blk * per;
+  }
   const uint32_t e = p.blocks[blk];
   U.b = static_cast<int>(e >> 16);
   U.qb = static_cast<int>(e & 0xFFFFu);

@@ -135,6 +135,18 @@ def test_gqa_packing_override_from_environment(lib, monkeypatch, value, ok):
         assert e.value.status == cp.E_INVALID
 
 
+@pytest.mark.parametrize("value,ok", [("auto", True), ("longest", True), ("kv_major", True),
+                                      ("kv", False)])
+def test_unit_order_override_from_environment(lib, monkeypatch, value, ok):
+    monkeypatch.setenv("CPATTN_UNIT_ORDER", value)
+    if ok:
+        cp.Context(8, 2, 128, 2, 64, 32).close()
+    else:
+        with pytest.raises(cp.CpattnError) as e:
+            cp.Context(8, 2, 128, 2, 64, 32)
+        assert e.value.status == cp.E_INVALID
+
+
 def test_no_multicast_tma_load_in_the_sources():
     """The library may be launched on several GPUs (one replica per GPU), so
     no TMA load in it may use cluster multicast; mbarrier signals

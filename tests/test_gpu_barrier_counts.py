@@ -187,9 +187,11 @@ def _check(w, mode, ctx, counts, totals=True):
     return tiles, units
 
 
+@pytest.mark.parametrize("order", ["longest", "kv_major"])
 @pytest.mark.parametrize("mode", ["mma2", "none", "pingpong"])
 @pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
-def test_barrier_counts_balance(w, mode, counted_lib):
+def test_barrier_counts_balance(w, mode, order, counted_lib, monkeypatch):
+    monkeypatch.setenv("CPATTN_UNIT_ORDER", order)
     ctx, counts = _run(w, mode, counted_lib)
     _check(w, mode, ctx, counts)
 

@@ -66,3 +66,28 @@ def test_pairing_modes_repeatable():
         for _ in range(3):
             dc.prefill(ctx)
             assert np.array_equal(first, dc.out.bits()), mode
+
+
+ORDER_CASES = [
+    # Several rounds of units on the persistent grid, more than one kv head.
+    small("ord128", (3000, 1500), (1024, 640), 1024, nq=32, nkv=4, hd=128, shards=8, seed=44),
+    small("ord256", (2500,), (1024,), 1024, nq=32, nkv=2, hd=256, shards=8, seed=45),
+]
+
+
+@pytest.mark.parametrize("order", ["longest", "kv_major"])
+@pytest.mark.parametrize("w", ORDER_CASES, ids=[w.name for w in ORDER_CASES])
+@pytest.mark.parametrize("mode", MODES)
+def test_unit_orders(mode, w, order, monkeypatch):
+    """Units dealt longest first or kv-head-major (CPATTN_UNIT_ORDER, a test
+    override of the cost model's choice): the same parity in every mode."""
+    monkeypatch.setenv("CPATTN_UNIT_ORDER", order)
+    case = make_case(w)
+    dc = DeviceCase(case)
+    dc.prefill(cp.Context.for_workload(w, pairing=mode))
+    ref, ref_lse = case.oracle_full()
+    v = dc.valid_rows()
+    compare(to_f64(dc.out.bits())[v], ref[v], f"{mode} {w.name} {order}")
+    lse = dc.lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse[v] - ref_lse[v])) < 2e-3, "LSE"
+    assert dc.guards_intact()
