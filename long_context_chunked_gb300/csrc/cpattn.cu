@@ -143,6 +143,20 @@ cpattn_status after_launch(cpattn_ctx* ctx, cudaStream_t stream, const char* wha
   return CPATTN_OK;
 }
 
+// The HD = 128 kernels move registers between warpgroups (setmaxnreg): the
+// two softmax warpgroups' increase waits until the third warpgroup's
+// decrease has freed enough of the CTA's launch-sized pool, which holds
+// exactly enough only if the kernel was compiled to kLaunchRegs registers
+// per thread.  A kernel built otherwise is never launched.
+bool register_split_ok(const void* kernel) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return fa.numRegs == cpattn::kLaunchRegs && fa.maxThreadsPerBlock >= cpattn::kThreads;
+}
+
 template <int HD, bool SPLIT, int MODE, bool VF16>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
   static_assert(MODE == 0 || MODE == 2 || (MODE == 3 && HD == 128),
@@ -162,6 +176,11 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(prefill)");
+    if (MODE != 3 && cpattn::Layout<HD>::SPLIT_O &&
+        !register_split_ok(reinterpret_cast<const void*>(kernel)))
+      return fail(ctx, CPATTN_E_UNSUPPORTED,
+                  "the HD = 128 prefill kernel was not built with the registers per thread "
+                  "its warpgroup register split assumes");
     grid_cap = ctx->num_sms;
     if (MC) {
       // Persistent grid of co-resident CTA pairs.
@@ -822,6 +841,8 @@ constexpr int kNoAllocMaxDevices = 64;
 // point launches it (plain launch, no cluster).
 template <int HD, bool SPLIT, bool VF16>
 cudaError_t noalloc_attr() {
+  const void* k = reinterpret_cast<const void*>(cpattn::prefill_kernel<HD, SPLIT, VF16>);
+  if (cpattn::Layout<HD>::SPLIT_O && !register_split_ok(k)) return cudaErrorInvalidDeviceFunction;
   return cudaFuncSetAttribute(cpattn::prefill_kernel<HD, SPLIT, VF16>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               cpattn::Layout<HD>::SMEM_BYTES);

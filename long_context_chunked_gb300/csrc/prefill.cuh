@@ -115,7 +115,20 @@ constexpr int kMmaWarp = kSoftmaxWarps + 1;
 // launch; it must not share a warp with the producer or the MMA thread, whose
 // waits its copy loop would otherwise serialise (measured: +7-24 % per step).
 constexpr int kWriterWarp = kSoftmaxWarps + 2;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+// The last warp only completes the third warpgroup (producer, MMA, writer,
+// idle), so that registers can move between whole warpgroups (HD = 128).
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
+// Registers per thread: the launch gives every thread kLaunchRegs (the
+// __launch_bounds__ cap for kThreads threads, checked on the host before the
+// first launch); at HD = 128 the two softmax warpgroups then take
+// kSoftmaxRegs and the third warpgroup keeps kOtherRegs -- exactly the
+// launch's pool, so the increase never waits for registers nobody frees.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 224;
+constexpr int kOtherRegs = 56;
+static_assert(kThreads == 384 && kThreads * kLaunchRegs <= 65536, "one CTA per SM");
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs == kThreads * kLaunchRegs,
+              "register split = launch allocation");
 constexpr uint32_t kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr uint32_t kRowGroupThreads = 32 * kColGroups;  // one named barrier per row group
 
@@ -141,9 +154,19 @@ struct Layout {
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_SFULL = 2, B_PFULL = 4, B_ODONE = 6,
                        B_DRAIN = 8, B_SLOTFULL = 9, B_SLOTEMPTY = 9 + NSLOT;
   static constexpr int NBAR = 9 + 2 * NSLOT;
+  // HD = 128: two O accumulators, and K/V tiles alternate between the two
+  // softmax warpgroups (whole rows per warp; softmax_role_rows).  TMEM:
+  // O_0 [0, 128), S_0 [128, 256), S_1 [256, 384), O_1 [384, 512).
+  static constexpr bool SPLIT_O = HD == 128;
+  static constexpr uint32_t O_COL1 = HD + 2 * kBKV;
+  // Softmax arrivals per tile on P_FULL (threads of the warps that take it).
+  static constexpr uint32_t P_THREADS = SPLIT_O ? kSoftmaxThreads / 2 : kSoftmaxThreads;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_XCH = OFF_MISC + 16;  // [kColGroups][128] fp32 row exchange
-  static constexpr int OFF_PFAIL = OFF_XCH + kColGroups * 128 * 4;  // [4] int: a row group gave up
+  // Row exchange, fp32: [kColGroups][128] maxima (HD = 256); [2][2][128]
+  // (m, l) of each warpgroup (HD = 128).
+  static constexpr int XCH_FLOATS = SPLIT_O ? 4 * 128 : kColGroups * 128;
+  static constexpr int OFF_XCH = OFF_MISC + 16;
+  static constexpr int OFF_PFAIL = OFF_XCH + XCH_FLOATS * 4;  // [4] int: a row group gave up
   // Slack for aligning the dynamic shared memory base to 1024 B; the kernel
   // checks at entry that its base needs no more (it is 0 in practice).
   static constexpr int ALIGN_SLACK = 512;
@@ -153,7 +176,7 @@ struct Layout {
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(kBQ, HD, true);
   static constexpr uint32_t IDESC_PV_F16 = make_idesc_f16(kBQ, HD, true);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(HD + 2 * kBKV <= TMEM_COLS, "TMEM budget");
+  static_assert(HD + 2 * kBKV + (SPLIT_O ? HD : 0) <= TMEM_COLS, "TMEM budget");
 };
 
 static_assert(sizeof(PrefillParams) <= 32764, "kernel parameter budget");
@@ -427,6 +450,10 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
     if (!wwait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
     tc_fence_after();
     const uint32_t p_tmem = tmem + HD + sb * kBKV;
+    // SPLIT_O: tile t accumulates into O_{t % 2}, and the unit's first tile
+    // of each parity overwrites it.
+    const uint32_t o_tmem = tmem + (Ly::SPLIT_O && sb ? Ly::O_COL1 : 0u);
+    const int w_acc = Ly::SPLIT_O ? (w >> 1) : w;
     for (int j = 0; j < Ly::VSUB; ++j) {
       if (!wwait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
       tc_fence_after();
@@ -440,10 +467,10 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
         const int e0 = j * Ly::VROWS + kk * 16;
         const uint32_t pa = p_tmem + 32 * (e0 >> 5) + ((e0 & 31) >> 1);
         if (F16) {
-          mma_ts(tmem, pa, bd, Ly::IDESC_PV_F16, (w | j | kk) != 0);
+          mma_ts(o_tmem, pa, bd, Ly::IDESC_PV_F16, (w_acc | j | kk) != 0);
         } else {
-          mma_ts(tmem, pa, bd, Ly::IDESC_PV, (w | j | kk) != 0);
-          if (SPLIT) mma_ts(tmem, pa + 16, bd, Ly::IDESC_PV, 1u);
+          mma_ts(o_tmem, pa, bd, Ly::IDESC_PV, (w_acc | j | kk) != 0);
+          if (SPLIT) mma_ts(o_tmem, pa + 16, bd, Ly::IDESC_PV, 1u);
         }
       }
       serialize();
@@ -586,6 +613,64 @@ __device__ __forceinline__ void store_row(const PrefillParams& p, const Unit& U,
         pk.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv_l, __uint_as_float(o[8 * v4 + 3]) * inv_l);
         pk.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv_l, __uint_as_float(o[8 * v4 + 5]) * inv_l);
         pk.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv_l, __uint_as_float(o[8 * v4 + 7]) * inv_l);
+        orow[ch * 4 + v4] = pk;
+      }
+    }
+  }
+  if (with_lse && valid && lse_out != nullptr)
+    lse_out[orow_i] = (m + __log2f(l_row)) * 0.69314718055994531f;
+}
+
+// One output row merged from two partial softmaxes: O = (w0 O_0 + w1 O_1) /
+// l_row over the columns [ocol0, ocol0 + OCOLS), O_0 at o0_tmem and O_1 at
+// o1_tmem (this warp's lanes); an O whose flag is off is not read (it holds
+// no product of this unit).  Outputs as store_row.
+template <int HD, int OCOLS>
+__device__ __forceinline__ void store_row_merged(const PrefillParams& p, const Unit& U, int row,
+                                                 int head, int ocol0, uint32_t o0_tmem,
+                                                 uint32_t o1_tmem, float w0, float w1, bool has0,
+                                                 bool has1, float m, float l_row, bool with_lse) {
+  const bool valid = row < U.c;
+  const float inv_l = 1.f / l_row;
+  const float a0 = w0 * inv_l, a1 = w1 * inv_l;
+  const bool partial = U.part >= 0;
+  const long long tok_g = static_cast<long long>(U.b) * p.C + row;
+  const long long orow_i =
+      (partial ? static_cast<long long>(U.part + (row - U.q0)) : tok_g) * p.nq + head;
+  const bool f32 = partial || p.out_f32 != 0;
+  float* lse_out = partial ? p.ws_lse : p.lse;
+  uint4* orow = reinterpret_cast<uint4*>(p.out + orow_i * HD + ocol0);
+  float4* orow32 = reinterpret_cast<float4*>((partial ? p.ws_o : reinterpret_cast<float*>(p.out)) +
+                                             orow_i * HD + ocol0);
+#pragma unroll 1
+  for (int ch = 0; ch < OCOLS / 32; ++ch) {
+    // One O buffer at a time through the same 32 registers.
+    uint32_t o[32];
+    float y[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) y[i] = 0.f;
+    if (has0) {
+      tmem_ld32_wait(o0_tmem + 32 * ch, o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(o[i]) * a0;
+    }
+    if (has1) {
+      tmem_ld32_wait(o1_tmem + 32 * ch, o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) y[i] = fmaf(__uint_as_float(o[i]), a1, y[i]);
+    }
+    if (valid && f32) {
+#pragma unroll
+      for (int v4 = 0; v4 < 8; ++v4)
+        orow32[ch * 8 + v4] = make_float4(y[4 * v4], y[4 * v4 + 1], y[4 * v4 + 2], y[4 * v4 + 3]);
+    } else if (valid) {
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) {
+        uint4 pk;
+        pk.x = pack_bf16x2(y[8 * v4 + 0], y[8 * v4 + 1]);
+        pk.y = pack_bf16x2(y[8 * v4 + 2], y[8 * v4 + 3]);
+        pk.z = pack_bf16x2(y[8 * v4 + 4], y[8 * v4 + 5]);
+        pk.w = pack_bf16x2(y[8 * v4 + 6], y[8 * v4 + 7]);
         orow[ch * 4 + v4] = pk;
       }
     }
@@ -836,6 +921,221 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
   }
 }
 
+// ------------------------------------------ softmax, HD = 128: whole rows
+// The two softmax warpgroups take alternate K/V tiles of a unit: warpgroup b
+// (warps 4b .. 4b+3, warp w reading TMEM lanes 32 (w % 4) ..) takes the tiles
+// whose CTA-wide index t has t % 2 == b, whole rows of them (128 logits per
+// thread), and keeps its own online softmax (m_b, l_b) and its own O_b in
+// TMEM, into which the MMA warp accumulates P_t V_t.  The two partial
+// softmaxes of a row are merged exactly at the unit's epilogue:
+//   m = max(m_0, m_1),  w_b = 2^(m_b - m),
+//   O = (w_0 O_0 + w_1 O_1) / (w_0 l_0 + w_1 l_1)
+// -- the same single softmax over all the unit's keys (a split of the sum,
+// not a second launch: both halves live in one CTA's TMEM).  No per-tile
+// exchange between warps is needed, each thread's per-tile work is spread
+// over twice the logits, and two tiles are in the softmax stage at once.
+// The row group (warps w and w + 4, one named barrier) meets only at the
+// epilogue.
+//
+// Ordering.  Warpgroup b observes every completion of S_FULL[b] (its
+// tiles), P.V completions on O_DONE[b] in order (tile t - 2's, the previous
+// product into O_b, before it works on tile t: complete already, since QK^T
+// of tile t was issued after it), and rescales O_b only then; P.V of tile t
+// is issued after its P arrival, so no product into O_b is in flight during
+// the rescale.  At the epilogue each warpgroup waits for its own last P.V,
+// then the row group meets, and meets again once both have read O_0 and O_1,
+// before either can arrive for the next unit's first tile (whose P.V
+// overwrites an O).
+template <bool SPLIT, bool PAIR2, bool VF16, int CL>
+__device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32_t sbase,
+                                                  uint32_t tmem, const BoundedWait& wait) {
+  constexpr int HD = 128;
+  using Ly = Layout<HD>;
+  static_assert(Ly::SPLIT_O && kColGroups == 2, "two warpgroups, two O accumulators");
+  auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  constexpr int CH = kBKV / 32;  // 32-column TMEM loads per row
+  const int warp = threadIdx.x >> 5;
+  const uint32_t b = static_cast<uint32_t>(warp >> 2);   // tile parity and O buffer
+  const int r = ((warp & 3) << 5) | (threadIdx.x & 31);  // row == TMEM lane
+  const uint32_t pair_bar = 1u + static_cast<uint32_t>(warp & 3);
+  const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(r & ~31) << 16);
+  const uint32_t s_tmem = lane_tmem + HD + b * kBKV;
+  float* xch = reinterpret_cast<float*>(__cvta_shared_to_generic(sbase + Ly::OFF_XCH));
+  volatile int* pair_fail = reinterpret_cast<volatile int*>(
+      __cvta_shared_to_generic(sbase + Ly::OFF_PFAIL)) + (warp & 3);
+  const float sl2 = p.scale_log2;
+  uint32_t tile_ctr = 0;  // CTA-wide tile index (the MMA warp's sequence)
+  bool drop_one = (p.debug_flags & kDebugDropArrive) && blockIdx.x == 0 && threadIdx.x == 0;
+
+  for (int ur = 0, u = unit_of<CL>(0); u < p.num_units; u = unit_of<CL>(++ur)) {
+    const Unit U = decode_unit(p, u);
+    const int tok = U.q0 + (p.packed ? r / p.group : r);
+    const int head = p.packed ? U.h + r % p.group : U.h;
+    CacheWalk walk;
+    walk.init(U.L, p.P, p.S);
+    walk.skip(U.v0 < U.n_cache ? U.v0 : U.n_cache);
+    float m = -INFINITY;  // this warpgroup's reference max (log2 units), per row
+    float l = 0.f;        // its running sum of 2^(x - m)
+    int mine = 0;         // tiles of this unit this warpgroup took
+    uint32_t t_mine = 0;  // the last of them
+    bool ok = true;
+
+    for (int v = 0; v < U.n_tiles; ++v) {
+      const uint32_t t = tile_ctr + static_cast<uint32_t>(v);
+      const int va = U.v0 + v;
+      const bool in_cache = va < U.n_cache;
+      // The walk advances over every cache tile, also the other warpgroup's.
+      const int tile = in_cache ? walk.next() : 0;
+      if ((t & 1u) != b || !ok) continue;
+      uint32_t mw[4];
+      if (in_cache) {
+        if (walk.last_full) {
+          mw[0] = mw[1] = mw[2] = mw[3] = 0xFFFFFFFFu;
+        } else {
+          walk.column_mask(tile, mw);
+        }
+      } else {
+        const int lim0 = tok - kBKV * (va - U.n_cache) + 1;
+        const int lim = lim0 < 0 ? 0 : (lim0 > kBKV ? kBKV : lim0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mw[q] = causal_word(lim, q);
+      }
+      const bool need_mask =
+          __any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu);
+      ok = __all_sync(0xFFFFFFFFu, wait(bar(Ly::B_SFULL + b), (t >> 1) & 1u, kSiteSFull));
+      // In order on O_DONE[b]: P.V of tile t - 2 (complete already).
+      if (ok && t >= 2)
+        ok = __all_sync(0xFFFFFFFFu, wait(bar(Ly::B_ODONE + b), ((t - 2) >> 1) & 1u, kSiteODone));
+      if (!ok) {
+        *pair_fail = 1;  // settled at the epilogue barrier
+        continue;
+      }
+      tc_fence_after();
+
+      // Pass 1: the row's 128 logits (all TMEM loads in flight together),
+      // masked by value, and their max.
+      uint32_t rr[CH][32];
+#pragma unroll
+      for (int c = 0; c < CH; ++c) tmem_ld32_async(s_tmem + 32 * c, rr[c]);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) tmem_ld32_fence(rr[c]);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            rr[c][i] = ((mw[c] >> i) & 1u) ? rr[c][i] : 0xFF800000u;  // -inf
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < CH; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(rr[c][i]));
+          mx1 = fmaxf(mx1, __uint_as_float(rr[c][i + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(rr[c][i + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(rr[c][i + 3]));
+        }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+
+      // Lazy rescale: the reference moves only when the row's new logits
+      // exceed it by more than 2^8 (the final O / l is the same either way).
+      const float m_new = fmaxf(m, m_tile);
+      const bool need = mine > 0 && m_new > m + 8.f;
+      const float alpha = need ? ex2_approx(m - m_new) : 1.f;
+      if (mine == 0 || need) m = m_new;
+
+      // Pass 2: p = 2^(x - m), its row sum, and P over the tile's S columns.
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 negm2 = make_float2(neg_m, neg_m);
+      float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
+      bool f16_done = false;
+      if constexpr (VF16) {
+        if (in_cache) {
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+            exp_pack_store<SPLIT, true>(rr[c], s_tmem + 32 * c, sl2x2, negm2, lsa, lsb);
+          f16_done = true;
+        }
+      }
+      if (!f16_done) {
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+          exp_pack_store<SPLIT, false>(rr[c], s_tmem + 32 * c, sl2x2, negm2, lsa, lsb);
+      }
+      l = l * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
+
+      // A row whose reference moved scales its O_b in place: every product
+      // into O_b so far (up to tile t - 2) is complete, and P.V of tile t
+      // waits for this warpgroup's arrival below.
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        const uint32_t o_tmem = lane_tmem + (b ? Ly::O_COL1 : 0u);
+#pragma unroll 1
+        for (int ch = 0; ch < HD / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32_wait(o_tmem + 32 * ch, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(o_tmem + 32 * ch, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      if (PAIR2) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+          if (drop_one) {
+            drop_one = false;  // fault-injection hook: this arrival never happens
+          } else {
+            count_arrive(p.bar_counts, 1u, Ly::B_PFULL + static_cast<int>(b), 1);
+            mbar_arrive_remote(mapa_shared(bar(Ly::B_PFULL + static_cast<int>(b)), 0));
+          }
+        }
+      } else if (drop_one) {
+        drop_one = false;  // fault-injection hook: this arrival never happens
+      } else {
+        count_arrive(p.bar_counts, 1u, Ly::B_PFULL + static_cast<int>(b), 1);
+        mbar_arrive(bar(Ly::B_PFULL + static_cast<int>(b)));
+      }
+      ++mine;
+      t_mine = t;
+    }
+    tile_ctr += static_cast<uint32_t>(U.n_tiles);
+
+    // Epilogue.  Each warpgroup waits for its own last P.V (in order on its
+    // O_DONE), posts (m_b, l_b), and the row group meets.
+    if (ok && mine > 0) {
+      ok = __all_sync(0xFFFFFFFFu,
+                      wait(bar(Ly::B_ODONE + b), (t_mine >> 1) & 1u, kSiteODone));
+      if (!ok) *pair_fail = 1;
+    }
+    xch[(2 * b) * 128 + r] = mine > 0 ? m : -INFINITY;
+    xch[(2 * b + 1) * 128 + r] = l;
+    tc_fence_before();
+    bar_sync(pair_bar, kRowGroupThreads);
+    if (*pair_fail) break;  // read by both warps after the same barrier
+    tc_fence_after();
+    const float m0 = xch[r], l0 = xch[128 + r];
+    const float m1 = xch[256 + r], l1 = xch[384 + r];
+    const float mm = fmaxf(m0, m1);
+    const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
+    const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+    const float l_row = w0 * l0 + w1 * l1;
+    // Which O buffers hold this unit's products (a one-tile unit has none in
+    // O_1, whose contents are then stale): uniform over the unit.
+    const bool has0 = U.n_tiles > 0 && (((tile_ctr - U.n_tiles) & 1u) == 0 || U.n_tiles > 1);
+    const bool has1 = U.n_tiles > 0 && (((tile_ctr - U.n_tiles) & 1u) == 1 || U.n_tiles > 1);
+    store_row_merged<HD, HD / 2>(p, U, tok, head, static_cast<int>(b) * (HD / 2),
+                                 lane_tmem + b * (HD / 2), lane_tmem + Ly::O_COL1 + b * (HD / 2),
+                                 has0 ? w0 : 0.f, has1 ? w1 : 0.f, has0, has1, mm, l_row, b == 0);
+    // Both warps are done reading O_0 and O_1 before either arrives for the
+    // next unit's first tile.
+    tc_fence_before();
+    bar_sync(pair_bar, kRowGroupThreads);
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <int HD, bool SPLIT, bool VF16>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
@@ -855,7 +1155,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Ly::NBAR; ++i)
-      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? kSoftmaxThreads : 1u);
+      mbar_init(bar(i), (i == Ly::B_PFULL || i == Ly::B_PFULL + 1) ? Ly::P_THREADS : 1u);
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) reinterpret_cast<volatile int*>(smem + Ly::OFF_PFAIL)[i] = 0;
     fence_mbar_init();
@@ -878,13 +1178,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const BoundedWait wait = make_wait(abort_flag, p, bar(0), warp);
 
   if (warp < kProducerWarp) {
-    softmax_role<HD, SPLIT, false, VF16, 1>(p, sbase, tmem, wait);
-  } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role<HD>(p, sbase, wait);
-  } else if (warp == kWriterWarp) {
-    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 1>(p, lane);
+    if constexpr (Ly::SPLIT_O) {
+      reg_alloc_inc<kSoftmaxRegs>();
+      softmax_role_rows<SPLIT, false, VF16, 1>(p, sbase, tmem, wait);
+    } else {
+      softmax_role<HD, SPLIT, false, VF16, 1>(p, sbase, tmem, wait);
+    }
   } else {
-    mma_role<HD, SPLIT, VF16>(p, sbase, tmem, wait);
+    if constexpr (Ly::SPLIT_O) reg_alloc_dec<kOtherRegs>();
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer_role<HD>(p, sbase, wait);
+    } else if (warp == kWriterWarp) {
+      if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 1>(p, lane);
+    } else if (warp == kMmaWarp) {
+      mma_role<HD, SPLIT, VF16>(p, sbase, tmem, wait);
+    }
   }
   __syncwarp();
   tc_fence_before();

@@ -46,7 +46,8 @@ struct PairLayout {
   static constexpr uint32_t IDESC_QK = make_idesc_bf16(2 * kBQ, kBKV, false);
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(2 * kBQ, HD, true);
   static constexpr uint32_t IDESC_PV_F16 = make_idesc_f16(2 * kBQ, HD, true);
-  static constexpr uint32_t P_ARRIVALS = 2 * kSoftmaxThreads / 32;
+  // One arrival per softmax warp of both CTAs that takes the tile.
+  static constexpr uint32_t P_ARRIVALS = 2 * Layout<HD>::P_THREADS / 32;
   static_assert(VCH * VRG * BOX == Layout<HD>::SUB, "V slot = 16 KB");
   static_assert(2 * BOX == Layout<HD>::SUB, "K slot = two chunks of 64 rows");
 };
@@ -207,6 +208,9 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
     if (!wwait(bar(Ly::B_PFULL + sb), (t >> 1) & 1u, kSitePFull)) return false;
     tc_fence_after();
     const uint32_t p_tmem = tmem + HD + sb * kBKV;
+    // SPLIT_O: tile t accumulates into O_{t % 2} (see prefill.cuh).
+    const uint32_t o_tmem = tmem + (Ly::SPLIT_O && sb ? Ly::O_COL1 : 0u);
+    const int w_acc = Ly::SPLIT_O ? (w >> 1) : w;
     for (int j = 0; j < Pl::VSLOTS; ++j) {
       if (!wwait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
       tc_fence_after();
@@ -219,10 +223,10 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
         const int e0 = j * Pl::VR + kk * 16;
         const uint32_t pa = p_tmem + 32 * (e0 >> 5) + ((e0 & 31) >> 1);
         if (F16) {
-          mma2_ts(tmem, pa, bd, Pl::IDESC_PV_F16, (w | j | kk) != 0);
+          mma2_ts(o_tmem, pa, bd, Pl::IDESC_PV_F16, (w_acc | j | kk) != 0);
         } else {
-          mma2_ts(tmem, pa, bd, Pl::IDESC_PV, (w | j | kk) != 0);
-          if (SPLIT) mma2_ts(tmem, pa + 16, bd, Pl::IDESC_PV, 1u);
+          mma2_ts(o_tmem, pa, bd, Pl::IDESC_PV, (w_acc | j | kk) != 0);
+          if (SPLIT) mma2_ts(o_tmem, pa + 16, bd, Pl::IDESC_PV, 1u);
         }
       }
       serialize();
@@ -342,13 +346,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const BoundedWait wait = make_wait(abort_flag, p, bar(0), warp);
 
   if (warp < kProducerWarp) {
-    softmax_role<HD, SPLIT, true, VF16, 2>(p, sbase, tmem, wait);
-  } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
-  } else if (warp == kWriterWarp) {
-    if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 2>(p, lane);
-  } else if (warp == kMmaWarp && rank == 0) {
-    mma_role_pair2<HD, SPLIT, VF16>(p, sbase, tmem, wait);
+    if constexpr (Ly::SPLIT_O) {
+      reg_alloc_inc<kSoftmaxRegs>();
+      softmax_role_rows<SPLIT, true, VF16, 2>(p, sbase, tmem, wait);
+    } else {
+      softmax_role<HD, SPLIT, true, VF16, 2>(p, sbase, tmem, wait);
+    }
+  } else {
+    if constexpr (Ly::SPLIT_O) reg_alloc_dec<kOtherRegs>();
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
+    } else if (warp == kWriterWarp) {
+      if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 2>(p, lane);
+    } else if (warp == kMmaWarp && rank == 0) {
+      mma_role_pair2<HD, SPLIT, VF16>(p, sbase, tmem, wait);
+    }
   }
   __syncwarp();
   tc_fence_before();

@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWriterWarp) {
     if (p.k_cache_w != nullptr)
       kv_write_units<Ly::HD, VF16>(p, lane, [](int i) { return unit_pingpong(i >> 1, i & 1); });
-  } else {
+  } else if (warp == kMmaWarp) {
     mma_role_pingpong<SPLIT, VF16>(p, sbase, tmem, wait);
   }
   __syncwarp();

@@ -183,6 +183,22 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return true;
 }
 
+// Register reallocation between warpgroups (every warp of a warpgroup
+// executes the same one): .inc waits until the CTA's pool, which the launch
+// sized at threads x registers per thread, has that many free per thread --
+// the other warpgroups' .dec must free them, so the shares of all
+// warpgroups may not add up to more than the launch allocation.
+template <int N>
+__device__ __forceinline__ void reg_alloc_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg operand");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg operand");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

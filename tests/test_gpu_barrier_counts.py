@@ -63,10 +63,12 @@ def _layout(form, hd):
     per_tile = {"single": hd // 64 + 128 // (8192 // hd), "pair2": 2 * (hd // 128),
                 "pingpong": 4}[form]
     count = np.ones(SLOTFULL + 2 * nslot, dtype=np.int64)
+    # HD = 128 (outside the two-tile kernel): one softmax warpgroup per tile.
+    takers = 4 if hd == 128 else 8
     if form == "single":
-        count[PFULL:PFULL + 2] = 256
+        count[PFULL:PFULL + 2] = 32 * takers
     elif form == "pair2":
-        count[PFULL:PFULL + 2] = 16
+        count[PFULL:PFULL + 2] = 2 * takers
         count[QFULL] = 2
         count[SLOTFULL:SLOTFULL + nslot] = 2
     else:
@@ -96,9 +98,26 @@ def _run(w, mode, counted_lib, split_tiles=None, fused_write=False):
     return ctx, counts
 
 
-def _check_cta(c, A, W, form, nslot, per_tile, count, leader=True):
-    """The per-CTA invariants; returns (tiles, units) of the CTA (the
-    leader's, in a pair)."""
+def _pv_waits_ok(W, tiles, units, hd, c):
+    """The softmax's in-order waits for P.V.  HD = 256: every softmax warp
+    waits for tile t - 2's product from the CTA's third tile on, and for each
+    unit's last product at its epilogue.  HD = 128: the warpgroup that takes
+    tile t waits for tile t - 2's, and at a unit's epilogue each warpgroup
+    that took a tile of it waits for its own last one (one or two per unit:
+    bounded here, counted exactly over all CTAs by the caller)."""
+    got = W[SOFTMAX][ODONE] + W[SOFTMAX][ODONE + 1]
+    if hd == 256:
+        assert got == 8 * (max(tiles - 2, 0) + units), f"CTA {c}: P.V waits"
+        return 0
+    base = 4 * max(tiles - 2, 0)
+    assert base + 4 * units <= got <= base + 8 * units, f"CTA {c}: P.V waits"
+    return got - base
+
+
+def _check_cta(c, A, W, form, nslot, per_tile, count, leader=True, hd=256):
+    """The per-CTA invariants; returns (tiles, units, epilogue P.V waits) of
+    the CTA (the leader's, in a pair)."""
+    sw = 4 if hd == 128 else 8  # softmax warps that wait for one S
     nb = SLOTFULL + 2 * nslot
     a = A[:nb]
     assert np.all(a % count == 0), f"CTA {c}: partial phase {a.tolist()} / {count.tolist()}"
@@ -113,9 +132,8 @@ def _check_cta(c, A, W, form, nslot, per_tile, count, leader=True):
         assert np.all(W[MMA] == 0), f"CTA {c}: the peer issues no MMA"
         units, tiles = ph[QEMPTY], ph[SFULL] + ph[SFULL + 1]
         for b in (0, 1):
-            assert W[SOFTMAX][SFULL + b] == 8 * ph[SFULL + b], f"CTA {c}: S waits"
-        assert W[SOFTMAX][ODONE] + W[SOFTMAX][ODONE + 1] == 8 * (max(tiles - 2, 0) + units), \
-            f"CTA {c}: P.V waits"
+            assert W[SOFTMAX][SFULL + b] == sw * ph[SFULL + b], f"CTA {c}: S waits"
+        _pv_waits_ok(W, tiles, units, hd, c)
         assert W[PRODUCER][QEMPTY] == max(units - 1, 0), f"CTA {c}: Q empty"
         assert np.array_equal(W[PRODUCER][SE:SE + nslot], np.maximum(ph[SE:SE + nslot] - 1, 0)), \
             f"CTA {c}: slot-empty waits"
@@ -127,12 +145,9 @@ def _check_cta(c, A, W, form, nslot, per_tile, count, leader=True):
         tiles = ph[SFULL] + ph[SFULL + 1]
         for b in (0, 1):
             assert ph[PFULL + b] == ph[SFULL + b] == ph[ODONE + b], f"CTA {c}: S/P/O parity {b}"
-            assert W[SOFTMAX][SFULL + b] == 8 * ph[SFULL + b], f"CTA {c}: S waits"
+            assert W[SOFTMAX][SFULL + b] == sw * ph[SFULL + b], f"CTA {c}: S waits"
             assert W[MMA][PFULL + b] == ph[PFULL + b], f"CTA {c}: P waits"
-        # The softmax waits for tile t-2's P.V from its third tile on, and for
-        # each unit's last P.V at the epilogue.
-        assert W[SOFTMAX][ODONE] + W[SOFTMAX][ODONE + 1] == 8 * (max(tiles - 2, 0) + units), \
-            f"CTA {c}: P.V waits"
+        epi = _pv_waits_ok(W, tiles, units, hd, c)
         assert W[RESCALE][ODONE] + W[RESCALE][ODONE + 1] <= 8 * tiles
     else:
         tiles = ph[SFULL]
@@ -149,7 +164,7 @@ def _check_cta(c, A, W, form, nslot, per_tile, count, leader=True):
         f"CTA {c}: slot-empty waits"
     assert ph[SLOTFULL:SE].sum() == tiles * per_tile, f"CTA {c}: slots per tile"
     assert a[DRAIN] == 1 and W[MMA][DRAIN] == 1, f"CTA {c}: final drain"
-    return tiles, units
+    return tiles, units, (epi if form != "pingpong" else 0)
 
 
 def _check(w, mode, ctx, counts, totals=True):
@@ -157,13 +172,13 @@ def _check(w, mode, ctx, counts, totals=True):
     nslot, per_tile, count = _layout(form, w.head_dim)
     ran = np.nonzero(counts[:, ARRIVE, :].sum(axis=1))[0]
     assert ran.size > 0
-    tiles = units = 0
+    tiles = units = epi = 0
     for c in ran:
         A, W = counts[c, ARRIVE], counts[c]
         if form == "pair2":
             leader = c % 2 == 0
             assert (c ^ 1) in ran, f"CTA {c} ran without its pair"
-            r = _check_cta(c, A, W, form, nslot, per_tile, count, leader)
+            r = _check_cta(c, A, W, form, nslot, per_tile, count, leader, w.head_dim)
             if leader:
                 # The release barriers are signalled to both CTAs alike.
                 peer = counts[c + 1, ARRIVE]
@@ -172,10 +187,12 @@ def _check(w, mode, ctx, counts, totals=True):
                     assert peer[i] == A[i], f"pair {c}: barrier {i}"
                 tiles += r[0]
                 units += r[1]
+                epi += r[2]
         else:
-            r = _check_cta(c, A, W, form, nslot, per_tile, count)
+            r = _check_cta(c, A, W, form, nslot, per_tile, count, hd=w.head_dim)
             tiles += r[0]
             units += r[1]
+            epi += r[2]
     if totals:
         # Whole walks: a row block (b, qb) has n_cache(b) + qb + 1 tiles; a
         # unit is one q head (single), a head pair (pair2, pingpong).
@@ -184,6 +201,10 @@ def _check(w, mode, ctx, counts, totals=True):
         n_cache = [len(ctx.cache_walk(L)[0]) for L in w.cache_lens]
         assert units == per_block * len(blocks)
         assert tiles == per_block * sum(n_cache[b] + qb + 1 for b, qb in blocks)
+        if w.head_dim == 128 and form != "pingpong":
+            # Epilogue waits: one per warp of each warpgroup that took a tile
+            # of the unit -- one warpgroup for a one-tile walk, else both.
+            assert epi == 4 * per_block * sum(min(n_cache[b] + qb + 1, 2) for b, qb in blocks)
     return tiles, units
 
 
