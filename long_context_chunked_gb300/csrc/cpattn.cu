@@ -475,9 +475,6 @@ static cpattn_status check_config(const cpattn_config& c) {
   if (c.head_dim != 128 && c.head_dim != 256) return CPATTN_E_UNSUPPORTED;
   // Work units are (row block, q head) and their count must fit the kernel's int.
   if (c.num_q_heads > 65535) return CPATTN_E_UNSUPPORTED;
-  // The cache walk addresses the P * S flat rows of one (sequence, kv head) in 32 bits.
-  if (static_cast<long long>(c.num_shards) * c.shard_capacity + cpattn::kBKV >= (1LL << 31))
-    return CPATTN_E_UNSUPPORTED;
   return CPATTN_OK;
 }
 

@@ -980,20 +980,13 @@ __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32
     uint32_t t_mine = 0;  // the last of them
     bool ok = true;
 
-    int walked = 0;  // tiles of this slice the walk has passed
-    // This warpgroup's tiles: v with (tile_ctr + v) % 2 == b.
-    for (int v = static_cast<int>((b ^ tile_ctr) & 1u); v < U.n_tiles; v += 2) {
+    for (int v = 0; v < U.n_tiles; ++v) {
       const uint32_t t = tile_ctr + static_cast<uint32_t>(v);
       const int va = U.v0 + v;
       const bool in_cache = va < U.n_cache;
-      int tile = 0;
-      if (in_cache) {
-        // Past the other warpgroup's tile (cache tiles precede current ones).
-        if (walked < v) walk.skip(v - walked);
-        tile = walk.next();
-        walked = v + 1;
-      }
-      if (!ok) continue;
+      // The walk advances over every cache tile, also the other warpgroup's.
+      const int tile = in_cache ? walk.next() : 0;
+      if ((t & 1u) != b || !ok) continue;
       uint32_t mw[4];
       if (in_cache) {
         if (walk.last_full) {

@@ -28,7 +28,7 @@ struct CacheWalk {
   int k;          // next tile index (flat rows [k*BKV, k*BKV + BKV))
   int k_last;     // last tile of shard s's range
   int prev_last;  // last tile emitted so far
-  int lo, hi;     // filled flat rows of shard s: [s*S, s*S + n_s); P*S < 2^31 (host check)
+  long long lo, hi;  // filled flat rows of shard s: [s*S, s*S + n_s)
   bool last_full;    // the tile returned by next() lies wholly inside [lo, hi)
 
   __host__ __device__ __forceinline__ void init(int L_, int P_, int S_) {
@@ -48,9 +48,9 @@ struct CacheWalk {
         s = P;
         return;
       }
-      const int a = s * S;
-      int first = a / kBKV;
-      const int last = (a + f - 1) / kBKV;
+      const long long a = static_cast<long long>(s) * S;
+      int first = static_cast<int>(a / kBKV);
+      const int last = static_cast<int>((a + f - 1) / kBKV);
       if (first <= prev_last) first = prev_last + 1;
       if (first <= last) {
         k = first;
@@ -85,7 +85,7 @@ struct CacheWalk {
   // column mask.
   __host__ __device__ __forceinline__ int next() {
     const int t = k;
-    const int r0 = t * kBKV;
+    const long long r0 = static_cast<long long>(t) * kBKV;
     last_full = r0 >= lo && r0 + kBKV <= hi;
     prev_last = t;
     if (k < k_last)
@@ -100,16 +100,16 @@ struct CacheWalk {
   // the filled prefix of its shard.
   __host__ __device__ __forceinline__ void column_mask(int tile, uint32_t (&w)[4]) const {
     w[0] = w[1] = w[2] = w[3] = 0u;
-    const int r0 = tile * kBKV;
-    const int r1 = r0 + kBKV;
-    const int s0 = r0 / S;
-    for (int sh = s0; sh < P && sh * S < r1; ++sh) {
-      const int a = sh * S;
-      const int b = a + shard_fill(L, P, sh);
-      const int lo = a > r0 ? a : r0;
-      const int hi = b < r1 ? b : r1;
+    const long long r0 = static_cast<long long>(tile) * kBKV;
+    const long long r1 = r0 + kBKV;
+    int s0 = static_cast<int>(r0 / S);
+    for (int sh = s0; sh < P && static_cast<long long>(sh) * S < r1; ++sh) {
+      const long long a = static_cast<long long>(sh) * S;
+      const long long b = a + shard_fill(L, P, sh);
+      const long long lo = a > r0 ? a : r0;
+      const long long hi = b < r1 ? b : r1;
       if (lo >= hi) continue;
-      const int c0 = lo - r0, c1 = hi - r0;  // [c0, c1)
+      const int c0 = static_cast<int>(lo - r0), c1 = static_cast<int>(hi - r0);  // [c0, c1)
       for (int q = 0; q < 4; ++q) {
         const int qa = q * 32, qb = qa + 32;
         const int x0 = c0 > qa ? c0 : qa, x1 = c1 < qb ? c1 : qb;
