@@ -419,23 +419,30 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   prm.scale_log2 = c.softmax_scale * 1.4426950408889634f;
   for (int b = 0; b < num_seqs; ++b)
     prm.seqs[b] = cpattn::SeqInfo{cache_lens[b], chunk_lens[b], plan.ncache[b], 0};
-  for (size_t i = 0; i < plan.blocks.size(); ++i) {
-    const cpattn::WorkBlock& w = plan.blocks[i];
-    prm.blocks[i] = (static_cast<uint32_t>(w.b) << 16) | static_cast<uint32_t>(w.qb);
-    prm.range[i] = (static_cast<uint32_t>(w.v0) << 16) | static_cast<uint32_t>(w.v1);
-    prm.part[i] = w.part;
-  }
-  prm.num_units = static_cast<int>(plan.blocks.size()) * (packed ? NKV : NQ);
-  prm.num_blocks = static_cast<int>(plan.blocks.size());
-  if (!packed) {
+  // Unit order (PrefillParams::per): kv-head-major takes one block entry per
+  // (row block, kv head), so it needs NKV times the entries.
+  const size_t nblk = plan.blocks.size();
+  bool kv_major = false;
+  if (!packed && NKV > 1 && NQ <= 16384 && nblk * NKV <= CPATTN_MAX_ROW_BLOCKS &&
+      ctx->unit_order != 1) {
     std::vector<int>& lens = ctx->block_lens;
     lens.clear();
     for (const cpattn::WorkBlock& b : plan.blocks) lens.push_back(b.v1 - b.v0);
     // Executors take units_per_block units of a block (q heads, or head pairs).
-    prm.kv_major = ctx->unit_order == 2 ||
-                   (ctx->unit_order == 0 &&
-                    cpattn::prefer_kv_major(lens, units_per_block / NKV, NKV, executors));
+    kv_major = ctx->unit_order == 2 ||
+               cpattn::prefer_kv_major(lens, units_per_block / NKV, NKV, executors);
   }
+  const int G = NQ / NKV;
+  const int reps = kv_major ? NKV : 1;
+  prm.per = kv_major ? G : (packed ? NKV : NQ);
+  for (int g = 0, i = 0; g < reps; ++g)
+    for (size_t j = 0; j < nblk; ++j, ++i) {
+      const cpattn::WorkBlock& w = plan.blocks[j];
+      prm.blocks[i] = cpattn::pack_block(w.b, w.qb, g * G);
+      prm.range[i] = (static_cast<uint32_t>(w.v0) << 16) | static_cast<uint32_t>(w.v1);
+      prm.part[i] = w.part;
+    }
+  prm.num_units = static_cast<int>(nblk * reps) * prm.per;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cpattn_status s = dispatch_prefill(ctx, &prm, st, packed);
@@ -969,7 +976,8 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   for (int i = 0; i < n; ++i) {
     const uint64_t work = 0xFFFFFFFFull - (keys[i] >> 32);  // whole walk: [0, n_cache + qb + 1)
     if (work > static_cast<uint64_t>(cpattn::kMaxVirtualTiles)) return CPATTN_E_UNSUPPORTED;
-    prm.blocks[i] = static_cast<uint32_t>(keys[i] & 0xFFFFFFFFull);
+    prm.blocks[i] = cpattn::pack_block(static_cast<int>((keys[i] >> 16) & 0xFFFFu),
+                                       static_cast<int>(keys[i] & 0xFFFFu), 0);
     prm.range[i] = static_cast<uint32_t>(work);
     prm.part[i] = -1;
   }
@@ -999,6 +1007,7 @@ extern "C" cpattn_status cpattn_prefill_noalloc(const cpattn_config* cfg, int32_
   prm.C = c.chunk_size;
   prm.debug_flags = 0;
   prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.per = NQ;
   prm.num_units = n * NQ;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

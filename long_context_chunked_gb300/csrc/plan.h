@@ -94,6 +94,15 @@ inline bool prefer_kv_major(const std::vector<int>& block_lens, int per_kv, int 
   return snake_makespan(kv, executors) * 100 <= snake_makespan(lf, executors) * 101;
 }
 
+// A work block entry of the kernel's table: sequence b (< 128), first unit
+// head hoff (< 16384), q block qb (< 2048: a launch has at most
+// CPATTN_MAX_ROW_BLOCKS row blocks).
+inline uint32_t pack_block(int b, int qb, int hoff) {
+  return (static_cast<uint32_t>(b) << 25) | (static_cast<uint32_t>(hoff) << 11) |
+         static_cast<uint32_t>(qb);
+}
+static_assert(CPATTN_MAX_SEQS <= 128 && CPATTN_MAX_ROW_BLOCKS <= 2048, "work block entry bits");
+
 struct WorkBlock {
   int b, qb, v0, v1;
   int part;  // -1: writes the output; else the first partial row of a piece

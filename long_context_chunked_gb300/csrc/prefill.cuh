@@ -64,11 +64,13 @@ struct PrefillParams {
   int* status;
   unsigned long long timeout_ns;
   int num_units, nq, nkv, group, P, S, C, debug_flags;
-  // Unit order: 0 -- unit u is q head (or packed kv head) u % per of work
-  // block u / per, blocks longest first; 1 (kv-head-major) -- all units of
-  // kv head 0 (every block, longest first), then kv head 1, ...: the units
-  // that run together read one kv head's K/V, which then stays in L2.
-  int kv_major, num_blocks;
+  // Units per work block: unit u is unit (u % per) of block u / per, i.e.
+  // q head (or, packed, kv head) hoff + u % per of that block.  Longest-first
+  // order: per = NQ (packed: NKV) and hoff = 0.  kv-head-major order (the
+  // units that run together read one kv head's K/V, which then stays in L2):
+  // one block per (row block, kv head), per = G and hoff = g * G, all of kv
+  // head 0's blocks first.
+  int per;
   // out_f32: O is written to `out` as fp32 (the two-launch variant's partial
   // results) instead of bf16.
   int out_f32;
@@ -89,7 +91,8 @@ struct PrefillParams {
   float* ws_o;    // split-KV pieces: fp32 O / l, [partial rows][NQ][HD]
   float* ws_lse;  // split-KV pieces: LSE, [partial rows][NQ]
   SeqInfo seqs[CPATTN_MAX_SEQS];
-  // Work blocks, longest first.  blocks[i] = (b << 16) | q block;
+  // Work blocks in dealing order.  blocks[i] = (b << 25) | (hoff << 11) |
+  // q block (b < 128 sequences, hoff < 16384, q block < 2048);
   // range[i] = (v0 << 16) | v1: the slice [v0, v1) of the block's virtual tile
   // walk (its n_cache cache tiles, then its causal current tiles 0..qb);
   // part[i] = -1 when the block writes the final output, else the first
@@ -191,22 +194,12 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u) {
   Unit U;
-  const int per = p.packed ? p.nkv : p.nq;  // units per work block
-  int blk, k;
-  if (p.kv_major) {
-    const int gu = per / p.nkv;               // units of one kv head per block
-    const int span = p.num_blocks * gu;       // units of one kv head
-    const int g = u / span;
-    const int rem = u - g * span;
-    blk = rem / gu;
-    k = g * gu + (rem - blk * gu);
-  } else {
-    blk = u / per;
-    k = u - blk * per;
-  }
+  const int per = p.per;
+  const int blk = u / per;
   const uint32_t e = p.blocks[blk];
-  U.b = static_cast<int>(e >> 16);
-  U.qb = static_cast<int>(e & 0xFFFFu);
+  const int k = static_cast<int>((e >> 11) & 0x3FFFu) + (u - blk * per);
+  U.b = static_cast<int>(e >> 25);
+  U.qb = static_cast<int>(e & 0x7FFu);
   U.g = p.packed ? k : k / p.group;
   U.h = p.packed ? k * p.group : k;
   U.q0 = U.qb * (p.packed ? p.tb : kBQ);
