@@ -931,14 +931,17 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 // epilogue.
 //
 // Ordering.  Warpgroup b observes every completion of S_FULL[b] (its
-// tiles), P.V completions on O_DONE[b] in order (tile t - 2's, the previous
-// product into O_b, before it works on tile t: complete already, since QK^T
-// of tile t was issued after it), and rescales O_b only then; P.V of tile t
-// is issued after its P arrival, so no product into O_b is in flight during
-// the rescale.  At the epilogue each warpgroup waits for its own last P.V,
-// then the row group meets, and meets again once both have read O_0 and O_1,
-// before either can arrive for the next unit's first tile (whose P.V
-// overwrites an O).
+// tiles).  Tile t - 2's P.V, the previous product into O_b, is complete by
+// then: one thread issues every MMA, QK^T of tile t after that P.V, and a
+// commit arrives only once all of the thread's earlier MMAs are complete.
+// So O_b may be rescaled during tile t without a wait on O_DONE[b]; P.V of
+// tile t is issued after its P arrival, so no product into O_b is in flight
+// during the rescale.  O_DONE[b] is waited for only at the epilogue, for the
+// warpgroup's last P.V of the unit: every earlier phase of it is complete
+// then, so the parity wait is never more than one phase behind.  The row
+// group then meets, and meets again once both have read O_0 and O_1, before
+// either can arrive for the next unit's first tile (whose P.V overwrites an
+// O).
 template <bool SPLIT, bool PAIR2, bool VF16, int CL>
 __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32_t sbase,
                                                   uint32_t tmem, const BoundedWait& wait) {
@@ -996,9 +999,6 @@ __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32
       const bool need_mask =
           __any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu);
       ok = __all_sync(0xFFFFFFFFu, wait(bar(Ly::B_SFULL + b), (t >> 1) & 1u, kSiteSFull));
-      // In order on O_DONE[b]: P.V of tile t - 2 (complete already).
-      if (ok && t >= 2)
-        ok = __all_sync(0xFFFFFFFFu, wait(bar(Ly::B_ODONE + b), ((t - 2) >> 1) & 1u, kSiteODone));
       if (!ok) {
         *pair_fail = 1;  // settled at the epilogue barrier
         continue;
@@ -1060,8 +1060,9 @@ __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32
       l = l * alpha + ((lsa.x + lsa.y) + (lsb.x + lsb.y));
 
       // A row whose reference moved scales its O_b in place: every product
-      // into O_b so far (up to tile t - 2) is complete, and P.V of tile t
-      // waits for this warpgroup's arrival below.
+      // into O_b so far (up to tile t - 2) is complete (S_FULL of tile t was
+      // committed after it), and P.V of tile t waits for this warpgroup's
+      // arrival below.
       if (__any_sync(0xFFFFFFFFu, need)) {
         const uint32_t o_tmem = lane_tmem + (b ? Ly::O_COL1 : 0u);
 #pragma unroll 1
@@ -1096,8 +1097,9 @@ __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32
     }
     tile_ctr += static_cast<uint32_t>(U.n_tiles);
 
-    // Epilogue.  Each warpgroup waits for its own last P.V (in order on its
-    // O_DONE), posts (m_b, l_b), and the row group meets.
+    // Epilogue.  Each warpgroup waits for its own last P.V on its O_DONE
+    // (the only phase of it that can still be open), posts (m_b, l_b), and
+    // the row group meets.
     if (ok && mine > 0) {
       ok = __all_sync(0xFFFFFFFFu,
                       wait(bar(Ly::B_ODONE + b), (t_mine >> 1) & 1u, kSiteODone));

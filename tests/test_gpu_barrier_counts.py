@@ -99,19 +99,19 @@ def _run(w, mode, counted_lib, split_tiles=None, fused_write=False):
 
 
 def _pv_waits_ok(W, tiles, units, hd, c):
-    """The softmax's in-order waits for P.V.  HD = 256: every softmax warp
-    waits for tile t - 2's product from the CTA's third tile on, and for each
-    unit's last product at its epilogue.  HD = 128: the warpgroup that takes
-    tile t waits for tile t - 2's, and at a unit's epilogue each warpgroup
-    that took a tile of it waits for its own last one (one or two per unit:
-    bounded here, counted exactly over all CTAs by the caller)."""
+    """The softmax's waits for P.V.  HD = 256: every softmax warp waits in
+    order for tile t - 2's product from the CTA's third tile on, and for each
+    unit's last product at its epilogue.  HD = 128: only at a unit's
+    epilogue, where each warpgroup that took a tile of it waits for its own
+    last one (one or two per unit: bounded here, counted exactly over all
+    CTAs by the caller); tile t - 2's product is complete once S of tile t
+    is, so the tile loop waits for none."""
     got = W[SOFTMAX][ODONE] + W[SOFTMAX][ODONE + 1]
     if hd == 256:
         assert got == 8 * (max(tiles - 2, 0) + units), f"CTA {c}: P.V waits"
         return 0
-    base = 4 * max(tiles - 2, 0)
-    assert base + 4 * units <= got <= base + 8 * units, f"CTA {c}: P.V waits"
-    return got - base
+    assert 4 * units <= got <= 8 * units, f"CTA {c}: P.V waits"
+    return got
 
 
 def _check_cta(c, A, W, form, nslot, per_tile, count, leader=True, hd=256):
