@@ -159,6 +159,7 @@ class DeviceState:
         inp = generate(w)
         self.inp = inp
         self.ctx = cp.Context.for_workload(w, fast_p=fast_p, v_cache_f16=v_f16, pairing=pairing)
+        stage_v(self.ctx, w.num_seqs, device)
         self.q = inp.q.to(device)
         self.k_new = inp.k_new.to(device)
         self.v_new = inp.v_new.to(device)
@@ -495,6 +496,7 @@ def run_cumulative(contexts, fast_p=False, seed=7, v_f16=False, emit=True):
         kc = torch.zeros((1, NKV, P, S, HD), dtype=torch.bfloat16, device=dev)
         vc = torch.zeros_like(kc, dtype=torch.float16 if v_f16 else torch.bfloat16)
         ctx = cp.Context(NQ, NKV, HD, P, S, C, 0.0, fast_p, v_f16)
+        stage_v(ctx, 1, dev)
         chunks = n // C
 
         def request():
@@ -567,6 +569,7 @@ def run_splitkv(fast_p=False, reps=20, seed=11, v_f16=False):
             torch.float16 if v_f16 else torch.bfloat16).to(dev)
         out = torch.empty_like(q)
         ctx = cp.Context(NQ, NKV, HD, P, S, C, 0.0, fast_p, v_f16)
+        stage_v(ctx, B, dev)
         need, blocks = ctx.splitkv_workspace(cl, ch, 0)
         ws = torch.empty(max(need // 4, 64), dtype=torch.float32, device=dev)
 
@@ -643,8 +646,27 @@ def run_splitkv(fast_p=False, reps=20, seed=11, v_f16=False):
         del q, kn, vn, kc, vc, out, ws, ctx
 
 
+# fp16 V cache: stage the chunk's V in fp16 (cpattn_set_v_staging) so that
+# every tile takes fp16 P with one P.V product (--v-staging off: current
+# tiles keep the bf16 hi+lo pair, or fast_p).
+V_STAGING = True
+
+
+def stage_v(ctx, num_seqs: int, device):
+    """Register a V staging buffer for batches of up to num_seqs sequences
+    on an fp16-V-cache context (kept alive on the context)."""
+    import torch
+    if not (ctx.v_cache_f16 and V_STAGING):
+        return
+    n = ctx.v_staging_bytes(num_seqs)
+    ctx.v_stage_buf = torch.empty(n // 2, dtype=torch.float16, device=device)
+    ctx.set_v_staging(ctx.v_stage_buf)
+
+
 def precision_label(fast_p: bool, v_f16: bool) -> str:
     cur = "P rounded to bf16" if fast_p else "bf16 hi+lo P pair"
+    if v_f16 and V_STAGING:
+        return "every tile: fp16 P x fp16 V (the chunk's V staged in fp16)"
     if v_f16:
         return f"cache tiles: fp16 P x fp16 V; current tiles: {cur}"
     return "fast_p (P rounded to bf16)" if fast_p else "accurate P (bf16 hi+lo pair)"
@@ -666,6 +688,9 @@ def main():
                     help="V cache format (default f16: cache tiles take P in fp16, one P.V "
                          "product at the accurate mode's precision; bf16: the bf16 hi+lo P "
                          "pair on every tile)")
+    ap.add_argument("--v-staging", default="on", choices=["on", "off"],
+                    help="fp16 V cache: stage the chunk's V in fp16 so that its tiles take "
+                         "fp16 P too (default on; off: the bf16 hi+lo pair on current tiles)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", default="fused", choices=["fused", "two_launch", "fused_write"],
                     help="fused_write: the KV write inside the prefill launch; "
@@ -681,6 +706,8 @@ def main():
                     help="only the headline workload: skip the other configs, the bf16 V "
                          "cache record, the cumulative requests and the same-run peaks")
     args = ap.parse_args()
+    global V_STAGING
+    V_STAGING = args.v_staging == "on"
     world, rank, local = dist_setup()
     if args.splitkv:
         run_splitkv(fast_p=args.fast_p, v_f16=args.v_cache == "f16")

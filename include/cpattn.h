@@ -76,7 +76,10 @@ typedef struct {
                               P.V product (11-bit P, relative RMS error about
                               1.7e-3 on N(0,1) inputs, as the bf16 hi + lo
                               pair) at the cost of fast_p.  Current-chunk tiles
-                              still read bf16 v_new and follow fast_p. */
+                              read bf16 v_new and follow fast_p -- unless a V
+                              staging buffer is registered
+                              (cpattn_set_v_staging): the chunk's V is then
+                              staged in fp16 and its tiles take fp16 P too. */
   int32_t pairing;         /* how prefill pairs adjacent q heads of one kv
                               head when NQ/NKV is even (results meet the same
                               accuracy in every form; the bits may differ):
@@ -169,18 +172,24 @@ cpattn_status cpattn_write_kv(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* 
  * instead of one row of it.
  * Precision of P in P.V: with a bf16 V cache, P is carried as a bf16 hi + lo
  * pair (fast_p: P rounded once to bf16); with an fp16 V cache, cache tiles
- * take P in fp16 against the fp16 V and current-chunk tiles follow fast_p.
+ * take P in fp16 against the fp16 V, and current-chunk tiles follow fast_p
+ * -- or, with a V staging buffer registered (cpattn_set_v_staging), take P
+ * in fp16 against the chunk's V staged in fp16: a kernel that converts the
+ * valid rows of v_new (as cpattn_write_kv converts them; a value beyond
+ * 65504 is reported by cpattn_sync_status as CPATTN_E_RANGE) runs first on
+ * the stream.
  * Work units (one q head, or a pair, of one row block) go to a persistent
  * grid longest first; when the batch has several rounds of units and more
  * than one kv head, they may instead go kv-head-major (every unit of kv head
  * 0, then of kv head 1, ...) so that the units running together share one
  * kv head's K/V in L2 -- chosen when a model of the grid says it costs at
  * most 1 % of the time.  Results meet the same accuracy in either order.
- * One kernel launch -- unless a split-KV workspace is registered
- * (cpattn_set_splitkv) and the batch's plan cuts some walks, in which case a
- * second, merge kernel follows on the same stream.
- * Errors: E_INVALID (also: the registered split-KV workspace is smaller than
- * the plan needs), E_UNSUPPORTED (more than CPATTN_MAX_ROW_BLOCKS row blocks,
+ * One kernel launch -- preceded by the V staging kernel when a V staging
+ * buffer is registered, and followed by a merge kernel on the same stream
+ * when a split-KV workspace is registered (cpattn_set_splitkv) and the
+ * batch's plan cuts some walks.
+ * Errors: E_INVALID (also: the registered split-KV workspace or V staging
+ * buffer is smaller than the batch needs), E_UNSUPPORTED (more than CPATTN_MAX_ROW_BLOCKS row blocks,
  * a walk of more than 65535 tiles), E_CUDA.  A device-side timeout is
  * reported by cpattn_sync_status.
  */
@@ -263,6 +272,37 @@ cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
  */
 cpattn_status cpattn_set_splitkv(cpattn_ctx* ctx, void* workspace, uint64_t workspace_bytes,
                                  int32_t max_split_tiles);
+
+/*
+ * fp16 V cache: register a device buffer owned by the caller in which
+ * cpattn_prefill, cpattn_prefill_write_kv and cpattn_prefill_two_launch stage
+ * the chunk's V in fp16 before their prefill kernels, so that every tile,
+ * not only the cache's, takes P in fp16 with one P.V product (the cache's
+ * tiles already read fp16 V).  The staging is a second kernel on the same
+ * stream: valid rows of v_new converted to fp16 (round to nearest even,
+ * exact for 2^-17 <= |v| <= 65504, as cpattn_write_kv converts them; a
+ * value beyond 65504 is reported by cpattn_sync_status as CPATTN_E_RANGE),
+ * pad rows written as zeros.
+ *   buffer   device memory, 16-byte aligned, [num_seqs * C, NKV, HD] fp16
+ *            for the largest batch, used by every later prefill of this
+ *            context until replaced; NULL (the default) turns staging off.
+ *            Calls that overlap on the GPU must not share one buffer.
+ *   bytes    its size; a prefill whose batch needs more fails with
+ *            E_INVALID (query the need with cpattn_v_staging_bytes)
+ * cpattn_prefill_noalloc never stages (its current tiles keep the bf16 hi +
+ * lo pair, or fast_p).
+ * Errors: E_INVALID (NULL ctx; a buffer for a context whose V cache is
+ * bf16; a misaligned buffer).
+ */
+cpattn_status cpattn_set_v_staging(cpattn_ctx* ctx, void* buffer, uint64_t bytes);
+
+/*
+ * Bytes of the V staging buffer for a batch of num_seqs sequences:
+ * num_seqs * C * NKV * HD * 2, written to *bytes.  Host only.
+ * Errors: E_INVALID (NULL ctx or bytes, num_seqs outside
+ * [1, CPATTN_MAX_SEQS]).
+ */
+cpattn_status cpattn_v_staging_bytes(const cpattn_ctx* ctx, int32_t num_seqs, uint64_t* bytes);
 
 /*
  * Workspace bytes the split-KV plan of this batch needs under the policy

@@ -26,7 +26,7 @@ EXPORTS = ("cpattn_create", "cpattn_write_kv", "cpattn_prefill", "cpattn_sync_st
            "cpattn_status_string", "cpattn_last_error", "cpattn_prefill_noalloc",
            "cpattn_two_launch_workspace", "cpattn_prefill_two_launch", "cpattn_set_splitkv",
            "cpattn_splitkv_workspace", "cpattn_cache_walk_from", "cpattn_prefill_write_kv",
-           "cpattn_set_barrier_counts")
+           "cpattn_set_barrier_counts", "cpattn_set_v_staging", "cpattn_v_staging_bytes")
 
 # cpattn_config.pairing values, by name.
 PAIRING = {"mma2": 0, "none": 1, "pingpong": 2}
@@ -98,6 +98,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.cpattn_prefill_write_kv.restype = I32
     lib.cpattn_set_barrier_counts.argtypes = [P, P, ctypes.c_uint64]
     lib.cpattn_set_barrier_counts.restype = I32
+    if hasattr(lib, "cpattn_set_v_staging"):  # absent from older builds (A/B timing only)
+        lib.cpattn_set_v_staging.argtypes = [P, P, ctypes.c_uint64]
+        lib.cpattn_set_v_staging.restype = I32
+        lib.cpattn_v_staging_bytes.argtypes = [P, I32, ctypes.POINTER(ctypes.c_uint64)]
+        lib.cpattn_v_staging_bytes.restype = I32
     _libs[path] = lib
     return lib
 
@@ -236,6 +241,20 @@ class Context:
         self._check(self.lib.cpattn_splitkv_workspace(self._h, len(cl), clp, chp, max_split_tiles,
                                                       ctypes.byref(n), ctypes.byref(blocks)))
         return n.value, blocks.value
+
+    def set_v_staging(self, buffer=None):
+        """fp16 V cache: register a device buffer (a CUDA tensor, 16-byte
+        aligned, v_staging_bytes(num_seqs) bytes for the largest batch) in
+        which the prefill calls stage the chunk's V in fp16, or None to stop
+        staging."""
+        nbytes = 0 if buffer is None else buffer.numel() * buffer.element_size()
+        self._check(self.lib.cpattn_set_v_staging(self._h, _ptr(buffer), nbytes))
+
+    def v_staging_bytes(self, num_seqs: int) -> int:
+        """Bytes of the V staging buffer for a batch of num_seqs sequences."""
+        n = ctypes.c_uint64()
+        self._check(self.lib.cpattn_v_staging_bytes(self._h, num_seqs, ctypes.byref(n)))
+        return n.value
 
     def sync_status(self, stream=None) -> int:
         """Synchronise and return the status code (E_TIMEOUT if a device wait expired)."""

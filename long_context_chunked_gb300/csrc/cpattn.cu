@@ -35,7 +35,8 @@ struct cpattn_ctx {
   int device = -1;
   int num_sms = 0;
   int* d_status = nullptr;           // device status word (timeouts)
-  int grid_cap[2][2][4][2] = {};  // [HD == 256][split P][pairing mode][fp16 V cache]: 0 until set up
+  // [HD == 256][split P][pairing mode][V form: kVBf16, kVF16Cache, kVF16All]: 0 until set up
+  int grid_cap[2][2][4][3] = {};
   // Head pairing for even group sizes (cpattn_config.pairing, or the
   // CPATTN_PAIRING override): 2 = 2-SM MMA pairs, 3 = two query tiles per CTA
   // (HD = 128; 2 at HD = 256), 0 = off.
@@ -44,6 +45,11 @@ struct cpattn_ctx {
   // kSplitAuto, or a forced piece length in tiles); off until registered.
   void* split_ws = nullptr;
   size_t split_ws_bytes = 0;
+  // fp16 V cache: a caller-owned device buffer where the prefill entry
+  // points stage the chunk's V in fp16 (cpattn_set_v_staging); none: the
+  // chunk's tiles take the bf16 hi+lo P pair against bf16 V_new.
+  void* v_stage = nullptr;
+  size_t v_stage_bytes = 0;
   int split_policy = cpattn::kSplitOff;
   // GQA packing for short-chunk launches (cpattn_config.gqa_packing, or the
   // CPATTN_GQA_PACKING override).
@@ -157,7 +163,7 @@ bool register_split_ok(const void* kernel) {
   return fa.numRegs == cpattn::kLaunchRegs && fa.maxThreadsPerBlock >= cpattn::kThreads;
 }
 
-template <int HD, bool SPLIT, int MODE, bool VF16>
+template <int HD, bool SPLIT, int MODE, int VF16>
 cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t stream) {
   static_assert(MODE == 0 || MODE == 2 || (MODE == 3 && HD == 128),
                 "pairing modes: 0 (none), 2 (2-SM MMA pairs), 3 (two query tiles, HD = 128)");
@@ -271,31 +277,46 @@ int pack_block_tokens(const cpattn_ctx* ctx, int32_t num_seqs, const int32_t* ch
   return kBQ / G;
 }
 
-template <int HD, bool VF16>
+template <int HD, int VF16>
 cpattn_status dispatch_prefill_hd(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st,
                                   bool split, int mode) {
-  if constexpr (HD == 128) {
-    if (mode == 3) return split ? launch_prefill<HD, true, 3, VF16>(ctx, prm, st)
-                                : launch_prefill<HD, false, 3, VF16>(ctx, prm, st);
+  if constexpr (VF16 == cpattn::kVF16All) {
+    // Every tile takes one fp16 product: the form has no fast_p variant.
+    if constexpr (HD == 128) {
+      if (mode == 3) return launch_prefill<HD, true, 3, VF16>(ctx, prm, st);
+    }
+    if (mode == 2) return launch_prefill<HD, true, 2, VF16>(ctx, prm, st);
+    return launch_prefill<HD, true, 0, VF16>(ctx, prm, st);
+  } else {
+    if constexpr (HD == 128) {
+      if (mode == 3) return split ? launch_prefill<HD, true, 3, VF16>(ctx, prm, st)
+                                  : launch_prefill<HD, false, 3, VF16>(ctx, prm, st);
+    }
+    if (mode == 2) return split ? launch_prefill<HD, true, 2, VF16>(ctx, prm, st)
+                                : launch_prefill<HD, false, 2, VF16>(ctx, prm, st);
+    return split ? launch_prefill<HD, true, 0, VF16>(ctx, prm, st)
+                 : launch_prefill<HD, false, 0, VF16>(ctx, prm, st);
   }
-  if (mode == 2) return split ? launch_prefill<HD, true, 2, VF16>(ctx, prm, st)
-                              : launch_prefill<HD, false, 2, VF16>(ctx, prm, st);
-  return split ? launch_prefill<HD, true, 0, VF16>(ctx, prm, st)
-               : launch_prefill<HD, false, 0, VF16>(ctx, prm, st);
 }
 
+// The V form of a launch: a bf16 V cache; an fp16 one with the chunk's V as
+// bf16 V_new; or with the chunk's V staged in fp16 (every tile one fp16
+// product, so the form needs no fast_p variant: it runs as the SPLIT one).
 cpattn_status dispatch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaStream_t st,
-                               bool packed) {
+                               bool packed, bool v_staged) {
   const int HD = ctx->cfg.head_dim;
-  const bool split = ctx->cfg.fast_p == 0;
+  const bool split = ctx->cfg.fast_p == 0 || v_staged;
   const bool vf16 = ctx->cfg.v_cache_f16 != 0;
   // Pair adjacent q heads of one kv head when the group size allows.
   const int mode = launch_pair_mode(ctx, packed);
-  if (HD == 256)
-    return vf16 ? dispatch_prefill_hd<256, true>(ctx, prm, st, split, mode)
-                : dispatch_prefill_hd<256, false>(ctx, prm, st, split, mode);
-  return vf16 ? dispatch_prefill_hd<128, true>(ctx, prm, st, split, mode)
-              : dispatch_prefill_hd<128, false>(ctx, prm, st, split, mode);
+  if (HD == 256) {
+    if (v_staged) return dispatch_prefill_hd<256, cpattn::kVF16All>(ctx, prm, st, split, mode);
+    return vf16 ? dispatch_prefill_hd<256, cpattn::kVF16Cache>(ctx, prm, st, split, mode)
+                : dispatch_prefill_hd<256, cpattn::kVBf16>(ctx, prm, st, split, mode);
+  }
+  if (v_staged) return dispatch_prefill_hd<128, cpattn::kVF16All>(ctx, prm, st, split, mode);
+  return vf16 ? dispatch_prefill_hd<128, cpattn::kVF16Cache>(ctx, prm, st, split, mode)
+              : dispatch_prefill_hd<128, cpattn::kVBf16>(ctx, prm, st, split, mode);
 }
 
 // Combine the split-KV pieces of every split row block into the output.
@@ -351,7 +372,8 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
                              const int32_t* chunk_lens, const void* q, const void* k_new,
                              const void* v_new, const void* k_cache, const void* v_cache,
                              void* out, float* lse, void* stream, int region, int out_f32,
-                             int split, bool write_kv = false) {
+                             int split, bool write_kv = false, const void* v_cur = nullptr,
+                             int cur_f16 = 0) {
   const cpattn_config& c = ctx->cfg;
   const int HD = c.head_dim, NQ = c.num_q_heads, NKV = c.num_kv_heads;
   static thread_local cpattn::WorkPlan plan;
@@ -380,12 +402,14 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   const uint64_t rb = static_cast<uint64_t>(HD) * 2;
   bool ok = encode3d(&prm.tm_q, q, HD, NQ, T, rb, rb * NQ, 64, 1, kBQ) &&
             encode3d(&prm.tm_k_new, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV) &&
-            encode3d(&prm.tm_v_new, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, vrows) &&
+            encode3d(&prm.tm_v_new, v_cur != nullptr ? v_cur : v_new, HD, NKV, T, rb, rb * NKV,
+                     64, 1, vrows) &&
             encode3d(&prm.tm_k_cache, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV) &&
             encode3d(&prm.tm_v_cache, v_cache, HD, 1, rows, rb, rb, 64, 1, vrows) &&
             encode3d(&prm.tm_k_new_h, k_new, HD, NKV, T, rb, rb * NKV, 64, 1, kBKV / 2) &&
             encode3d(&prm.tm_k_cache_h, k_cache, HD, 1, rows, rb, rb, 64, 1, kBKV / 2) &&
-            encode3d(&prm.tm_v_new_h, v_new, HD, NKV, T, rb, rb * NKV, 64, 1, 64) &&
+            encode3d(&prm.tm_v_new_h, v_cur != nullptr ? v_cur : v_new, HD, NKV, T, rb, rb * NKV,
+                     64, 1, 64) &&
             encode3d(&prm.tm_v_cache_h, v_cache, HD, 1, rows, rb, rb, 64, 1, 64) &&
             (!packed || encode3d(&prm.tm_q_packed, q, HD, NQ, T, rb, rb * NQ, 64,
                                  static_cast<uint32_t>(NQ / NKV), static_cast<uint32_t>(block_tokens)));
@@ -445,9 +469,52 @@ cpattn_status prefill_launch(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   prm.num_units = static_cast<int>(nblk * reps) * prm.per;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cpattn_status s = dispatch_prefill(ctx, &prm, st, packed);
+  cpattn_status s = dispatch_prefill(ctx, &prm, st, packed, cur_f16 != 0);
   if (s != CPATTN_OK || plan.groups.empty()) return s;
   return launch_splitkv_merge(ctx, plan, prm.ws_o, prm.ws_lse, out, lse, num_seqs, st);
+}
+
+// Bytes of the fp16 V staging buffer for a batch of num_seqs sequences:
+// the chunk's V in token order, [num_seqs * C, NKV, HD] fp16.
+uint64_t v_stage_need(const cpattn_config& c, int32_t num_seqs) {
+  return static_cast<uint64_t>(num_seqs) * c.chunk_size * c.num_kv_heads * c.head_dim * 2;
+}
+
+// fp16 V cache with a registered staging buffer: launch the staging of the
+// chunk's V (stage_v_f16_kernel) and point *v_cur at it, *cur_f16 = 1.
+// Otherwise *v_cur = v_new (bf16) and *cur_f16 = 0.
+cpattn_status stage_v(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* chunk_lens,
+                      const void* v_new, void* stream, const void** v_cur, int* cur_f16) {
+  const cpattn_config& c = ctx->cfg;
+  *v_cur = v_new;
+  *cur_f16 = 0;
+  if (!c.v_cache_f16 || ctx->v_stage == nullptr) return CPATTN_OK;
+  const uint64_t need = v_stage_need(c, num_seqs);
+  if (need > ctx->v_stage_bytes)
+    return fail(ctx, CPATTN_E_INVALID,
+                "the registered V staging buffer holds " + std::to_string(ctx->v_stage_bytes) +
+                    " bytes; this batch needs " + std::to_string(need) +
+                    " (cpattn_v_staging_bytes)");
+  if (ctx->d_status == nullptr) return fail(ctx, CPATTN_E_CUDA, "no CUDA device");
+  cpattn::StageVParams p;
+  p.v_new = static_cast<const uint4*>(v_new);
+  p.v_stage = static_cast<uint4*>(ctx->v_stage);
+  p.status = ctx->d_status;
+  p.C = c.chunk_size;
+  p.nkv = c.num_kv_heads;
+  p.vec_per_row = c.head_dim * 2 / 16;
+  p.total_vecs = static_cast<long long>(need / 16);
+  for (int b = 0; b < num_seqs; ++b) p.chunk_len[b] = chunk_lens[b];
+  const long long blocks = (p.total_vecs + 255) / 256;
+  const int grid =
+      static_cast<int>(std::min<long long>(blocks, static_cast<long long>(ctx->num_sms) * 16));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cpattn::stage_v_f16_kernel<<<grid, 256, 0, st>>>(p);
+  cpattn_status s = after_launch(ctx, st, "V staging launch");
+  if (s != CPATTN_OK) return s;
+  *v_cur = ctx->v_stage;
+  *cur_f16 = 1;
+  return CPATTN_OK;
 }
 
 }  // namespace
@@ -685,9 +752,14 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)))
     return fail(ctx, CPATTN_E_INVALID, "device pointers must be 16-byte aligned");
+  const void* v_cur = nullptr;
+  int cur_f16 = 0;
+  s = stage_v(ctx, num_seqs, chunk_lens, v_new, stream, &v_cur, &cur_f16);
+  if (s != CPATTN_OK) return s;
   return prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
                         out, lse, stream, cpattn::kRegionAll, 0,
-                        ctx->split_ws != nullptr ? ctx->split_policy : cpattn::kSplitOff);
+                        ctx->split_ws != nullptr ? ctx->split_policy : cpattn::kSplitOff, false,
+                        v_cur, cur_f16);
 }
 
 cpattn_status cpattn_prefill_write_kv(cpattn_ctx* ctx, int32_t num_seqs,
@@ -704,9 +776,14 @@ cpattn_status cpattn_prefill_write_kv(cpattn_ctx* ctx, int32_t num_seqs,
   if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
       !aligned16(v_cache) || !aligned16(out) || (lse != nullptr && !aligned16(lse)))
     return fail(ctx, CPATTN_E_INVALID, "device pointers must be 16-byte aligned");
+  const void* v_cur = nullptr;
+  int cur_f16 = 0;
+  s = stage_v(ctx, num_seqs, chunk_lens, v_new, stream, &v_cur, &cur_f16);
+  if (s != CPATTN_OK) return s;
   return prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
                         out, lse, stream, cpattn::kRegionAll, 0,
-                        ctx->split_ws != nullptr ? ctx->split_policy : cpattn::kSplitOff, true);
+                        ctx->split_ws != nullptr ? ctx->split_policy : cpattn::kSplitOff, true,
+                        v_cur, cur_f16);
 }
 
 cpattn_status cpattn_set_splitkv(cpattn_ctx* ctx, void* workspace, uint64_t workspace_bytes,
@@ -737,6 +814,24 @@ cpattn_status cpattn_splitkv_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
     return CPATTN_E_UNSUPPORTED;
   *bytes = cpattn::plan_workspace_bytes(plan, ctx->cfg.num_q_heads, ctx->cfg.head_dim);
   if (work_blocks != nullptr) *work_blocks = static_cast<int32_t>(plan.blocks.size());
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_set_v_staging(cpattn_ctx* ctx, void* buffer, uint64_t bytes) {
+  if (ctx == nullptr) return CPATTN_E_INVALID;
+  if (buffer != nullptr && !ctx->cfg.v_cache_f16)
+    return fail(ctx, CPATTN_E_INVALID, "V staging applies to an fp16 V cache only");
+  if (buffer != nullptr && !aligned16(buffer))
+    return fail(ctx, CPATTN_E_INVALID, "the V staging buffer must be 16-byte aligned");
+  ctx->v_stage = buffer;
+  ctx->v_stage_bytes = buffer != nullptr ? static_cast<size_t>(bytes) : 0;
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_v_staging_bytes(const cpattn_ctx* ctx, int32_t num_seqs, uint64_t* bytes) {
+  if (ctx == nullptr || bytes == nullptr || num_seqs < 1 || num_seqs > CPATTN_MAX_SEQS)
+    return CPATTN_E_INVALID;
+  *bytes = v_stage_need(ctx->cfg, num_seqs);
   return CPATTN_OK;
 }
 
@@ -790,12 +885,20 @@ cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
   float* o2 = reinterpret_cast<float*>(ws + off[1]);
   float* l1 = reinterpret_cast<float*>(ws + off[2]);
   float* l2 = reinterpret_cast<float*>(ws + off[3]);
-  // Launch 1: cache tiles only; launch 2: current tiles only (causal).
-  s = prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
-                     o1, l1, stream, cpattn::kRegionCache, 1, cpattn::kSplitOff);
+  // Launch 1: cache tiles only; launch 2: current tiles only (causal).  The
+  // tiles take the fused launch's forms (with a staged fp16 V, every tile
+  // fp16 P and one P.V product).
+  const void* v_cur = nullptr;
+  int cur_f16 = 0;
+  s = stage_v(ctx, num_seqs, chunk_lens, v_new, stream, &v_cur, &cur_f16);
   if (s != CPATTN_OK) return s;
   s = prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
-                     o2, l2, stream, cpattn::kRegionCurrent, 1, cpattn::kSplitOff);
+                     o1, l1, stream, cpattn::kRegionCache, 1, cpattn::kSplitOff, false, v_cur,
+                     cur_f16);
+  if (s != CPATTN_OK) return s;
+  s = prefill_launch(ctx, num_seqs, cache_lens, chunk_lens, q, k_new, v_new, k_cache, v_cache,
+                     o2, l2, stream, cpattn::kRegionCurrent, 1, cpattn::kSplitOff, false, v_cur,
+                     cur_f16);
   if (s != CPATTN_OK) return s;
   // Launch 3: LSE merge into bf16 O.
   cpattn::MergeParams m;

@@ -135,6 +135,14 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs == kThreads * kLaunchReg
 constexpr uint32_t kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr uint32_t kRowGroupThreads = 32 * kColGroups;  // one named barrier per row group
 
+// V forms of the prefill kernels (template parameter VF16): a bf16 V cache
+// (every tile: the bf16 hi + lo P pair, or fast P); an fp16 V cache with the
+// chunk's own V read as bf16 V_new (cache tiles: fp16 P and one P.V product;
+// current tiles as with a bf16 cache); an fp16 V cache with the chunk's V
+// staged in fp16 by the host (tm_v_new, tm_v_new_h point at the staging), so
+// that every tile takes fp16 P and one P.V product.
+enum : int { kVBf16 = 0, kVF16Cache = 1, kVF16All = 2 };
+
 // Sites recorded in the status word when a bounded wait expires.
 enum : int {
   kSiteQEmpty = 1, kSiteSlotEmpty, kSiteQFull, kSiteSlotFull, kSitePFull, kSiteSFull,
@@ -399,7 +407,7 @@ __device__ __forceinline__ void kv_write_lanes(const PrefillParams& p, int lane)
 // Run by the whole MMA warp: control flow and operands are warp-uniform (every
 // wait's outcome is agreed by the warp), and each MMA and commit is issued by
 // one elected lane.
-template <int HD, bool SPLIT, bool VF16>
+template <int HD, bool SPLIT, int VF16>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                          const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -475,7 +483,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, uint32_t sbase,
   };
   auto issue_pv = [&](const Unit& U, int w, uint32_t t) {
     if constexpr (VF16) {
-      if (U.v0 + w < U.n_cache) return issue_pv_as(w, t, std::true_type{});
+      if (VF16 == kVF16All || U.v0 + w < U.n_cache) return issue_pv_as(w, t, std::true_type{});
     }
     return issue_pv_as(w, t, std::false_type{});
   };
@@ -681,7 +689,7 @@ __device__ __forceinline__ void store_row_merged(const PrefillParams& p, const U
 // PAIR2: the CTA is one of a pair whose leader issues 2-SM MMAs; S, P and O
 // of this CTA's 128 rows sit in its own TMEM exactly as in a single CTA, but
 // "P ready" goes to the leader's barrier, one arrival per warp.
-template <int HD, bool SPLIT, bool PAIR2, bool VF16, int CL>
+template <int HD, bool SPLIT, bool PAIR2, int VF16, int CL>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sbase, uint32_t tmem,
                                              const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -825,7 +833,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
       {
         bool f16_done = false;
         if constexpr (VF16) {
-          if (in_cache) {
+          if (VF16 == kVF16All || in_cache) {
 #pragma unroll
             for (int c = 0; c < CH; ++c)
               exp_pack_store<SPLIT, true>(rr[c], s_tmem + 32 * c, sl2x2, negm2, lsa, lsb);
@@ -942,7 +950,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, uint32_t sb
 // group then meets, and meets again once both have read O_0 and O_1, before
 // either can arrive for the next unit's first tile (whose P.V overwrites an
 // O).
-template <bool SPLIT, bool PAIR2, bool VF16, int CL>
+template <bool SPLIT, bool PAIR2, int VF16, int CL>
 __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32_t sbase,
                                                   uint32_t tmem, const BoundedWait& wait) {
   constexpr int HD = 128;
@@ -1045,7 +1053,7 @@ __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32
       float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
       bool f16_done = false;
       if constexpr (VF16) {
-        if (in_cache) {
+        if (VF16 == kVF16All || in_cache) {
 #pragma unroll
           for (int c = 0; c < CH; ++c)
             exp_pack_store<SPLIT, true>(rr[c], s_tmem + 32 * c, sl2x2, negm2, lsa, lsb);
@@ -1132,7 +1140,7 @@ __device__ __forceinline__ void softmax_role_rows(const PrefillParams& p, uint32
 }
 
 // ------------------------------------------------------------------ kernel
-template <int HD, bool SPLIT, bool VF16>
+template <int HD, bool SPLIT, int VF16>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
   extern __shared__ uint8_t smem_raw[];
@@ -1184,7 +1192,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (warp == kProducerWarp) {
       if (lane == 0) producer_role<HD>(p, sbase, wait);
     } else if (warp == kWriterWarp) {
-      if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 1>(p, lane);
+      if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16 != kVBf16, 1>(p, lane);
     } else if (warp == kMmaWarp) {
       mma_role<HD, SPLIT, VF16>(p, sbase, tmem, wait);
     }

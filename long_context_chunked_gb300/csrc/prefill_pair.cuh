@@ -163,7 +163,7 @@ __device__ __forceinline__ void producer_role_pair2(const PrefillParams& p, uint
 // Leader CTA only, the whole MMA warp: control flow and operands are
 // warp-uniform (every wait's outcome is agreed by the warp), and each MMA and
 // commit is issued by one elected lane.
-template <int HD, bool SPLIT, bool VF16>
+template <int HD, bool SPLIT, int VF16>
 __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t sbase,
                                                uint32_t tmem, const BoundedWait& wait) {
   using Ly = Layout<HD>;
@@ -238,7 +238,7 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
   };
   auto issue_pv = [&](const Unit& U, int w, uint32_t t) {
     if constexpr (VF16) {
-      if (U.v0 + w < U.n_cache) return issue_pv_as(w, t, std::true_type{});
+      if (VF16 == kVF16All || U.v0 + w < U.n_cache) return issue_pv_as(w, t, std::true_type{});
     }
     return issue_pv_as(w, t, std::false_type{});
   };
@@ -296,7 +296,7 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
 // round of gridDim.x units (s = k in even rounds, E - 1 - k in odd ones:
 // unit_of), so the pair always holds q heads 2i and 2i + 1 of the same row
 // block (the host launches it only when the group size is even).
-template <int HD, bool SPLIT, bool VF16>
+template <int HD, bool SPLIT, int VF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel_pair2(const __grid_constant__ PrefillParams p) {
   using Ly = Layout<HD>;
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
       if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
     } else if (warp == kWriterWarp) {
-      if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16, 2>(p, lane);
+      if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16 != kVBf16, 2>(p, lane);
     } else if (warp == kMmaWarp && rank == 0) {
       mma_role_pair2<HD, SPLIT, VF16>(p, sbase, tmem, wait);
     }

@@ -157,7 +157,7 @@ __device__ __forceinline__ void producer_role_pingpong(const PrefillParams& p, u
 // ------------------------------------------------------------- MMA issuer
 // Run by the whole MMA warp (operands and control flow warp-uniform; each
 // MMA and commit is issued by one elected lane).
-template <bool SPLIT, bool VF16>
+template <bool SPLIT, int VF16>
 __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32_t sbase,
                                                   uint32_t tmem, const BoundedWait& wait) {
   using Ly = PingPongLayout;
@@ -252,7 +252,8 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
   // of the warp would cost every MMA a reconvergence.
   auto issue_pv = [&](const Unit& U, int q, RingPos rv, bool first, int w, uint32_t t) {
     if constexpr (VF16) {
-      if (U.v0 + w < U.n_cache) return issue_pv_as(q, rv, first, w, t, std::true_type{});
+      if (VF16 == kVF16All || U.v0 + w < U.n_cache)
+        return issue_pv_as(q, rv, first, w, t, std::true_type{});
     }
     return issue_pv_as(q, rv, first, w, t, std::false_type{});
   };
@@ -304,7 +305,7 @@ __device__ __forceinline__ void mma_role_pingpong(const PrefillParams& p, uint32
 // ------------------------------------------------------- softmax + epilogue
 // Warp w holds query tile q = w / 4 and its TMEM lane quarter w % 4: 32 whole
 // rows, all kBKV logits of each.
-template <bool SPLIT, bool VF16>
+template <bool SPLIT, int VF16>
 __device__ __forceinline__ void softmax_role_pingpong(const PrefillParams& p, uint32_t sbase,
                                                       uint32_t tmem, const BoundedWait& wait) {
   using Ly = PingPongLayout;
@@ -397,7 +398,7 @@ __device__ __forceinline__ void softmax_role_pingpong(const PrefillParams& p, ui
       float2 lsa = make_float2(0.f, 0.f), lsb = make_float2(0.f, 0.f);
       bool f16_done = false;
       if constexpr (VF16) {
-        if (in_cache) {
+        if (VF16 == kVF16All || in_cache) {
 #pragma unroll
           for (int c = 0; c < CH; ++c)
             exp_pack_store<SPLIT, true>(rr[c], s_tmem + 32 * c, sl2x2, negm2, lsa, lsb);
@@ -448,7 +449,7 @@ __device__ __forceinline__ void softmax_role_pingpong(const PrefillParams& p, ui
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool SPLIT, bool VF16>
+template <bool SPLIT, int VF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel_pingpong(const __grid_constant__ PrefillParams p) {
   using Ly = PingPongLayout;
@@ -494,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) producer_role_pingpong(p, sbase, wait);
   } else if (warp == kWriterWarp) {
     if (p.k_cache_w != nullptr)
-      kv_write_units<Ly::HD, VF16>(p, lane, [](int i) { return unit_pingpong(i >> 1, i & 1); });
+      kv_write_units<Ly::HD, VF16 != kVBf16>(p, lane,
+                                             [](int i) { return unit_pingpong(i >> 1, i & 1); });
   } else if (warp == kMmaWarp) {
     mma_role_pingpong<SPLIT, VF16>(p, sbase, tmem, wait);
   }

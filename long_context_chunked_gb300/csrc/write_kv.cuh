@@ -67,4 +67,39 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const __grid_constant__ W
   }
 }
 
+// The chunk's V in fp16, token order [B * C, NKV, HD] like V_new, for the
+// prefill of an fp16 V cache: its current tiles then take the same fp16 P
+// and single P.V product as its cache tiles.  Valid rows (token i < c_b) are
+// converted as the fp16 cache write converts them (a value beyond 65504 sets
+// kStatusRange); pad rows are written as zeros, so that a pad row's finite
+// but out-of-range bf16 value cannot become an infinity that a masked
+// (P = 0) column would turn into NaN.  HBM-bound: one 16-byte vector per
+// thread, coalesced.
+struct StageVParams {
+  const uint4* v_new;
+  uint4* v_stage;
+  int* status;
+  int C, nkv, vec_per_row;
+  long long total_vecs;  // B * C * NKV * vec_per_row
+  int chunk_len[CPATTN_MAX_SEQS];
+};
+
+__global__ void __launch_bounds__(256) stage_v_f16_kernel(const __grid_constant__ StageVParams p) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long per_token = static_cast<long long>(p.nkv) * p.vec_per_row;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+       idx < p.total_vecs; idx += stride) {
+    const long long token = idx / per_token;
+    const int b = static_cast<int>(token / p.C);
+    const int i = static_cast<int>(token - static_cast<long long>(b) * p.C);
+    uint4 vv = make_uint4(0u, 0u, 0u, 0u);
+    if (i < p.chunk_len[b]) {
+      bool overflow = false;
+      vv = bf16x8_to_f16x8(__ldg(p.v_new + idx), &overflow);
+      if (overflow && p.status != nullptr) atomicCAS(p.status, kStatusOk, kStatusRange);
+    }
+    p.v_stage[idx] = vv;
+  }
+}
+
 }  // namespace cpattn

@@ -297,6 +297,41 @@ def test_splitkv_workspace_too_small_is_refused_before_launch(lib):
     assert st == cp.E_INVALID and "split-KV workspace" in ctx.last_error()
 
 
+def test_v_staging_registration_checks(lib):
+    """Staging applies to an fp16 V cache only, and wants 16-byte alignment."""
+    bf = cp.Context(8, 2, 128, 2, 64, 32)
+    assert bf.lib.cpattn_set_v_staging(bf._h, 4096, 1 << 20) == cp.E_INVALID
+    assert "fp16 V cache only" in bf.last_error()
+    assert bf.lib.cpattn_set_v_staging(bf._h, None, 0) == cp.OK  # off is always fine
+    f16 = cp.Context(8, 2, 128, 2, 64, 32, v_cache_f16=True)
+    assert f16.lib.cpattn_set_v_staging(f16._h, 4096 + 8, 1 << 20) == cp.E_INVALID
+    assert f16.lib.cpattn_set_v_staging(f16._h, 4096, 1 << 20) == cp.OK
+    assert f16.lib.cpattn_set_v_staging(f16._h, None, 0) == cp.OK
+
+
+@pytest.mark.parametrize("num_seqs", [1, 3, 128])
+def test_v_staging_bytes(lib, num_seqs):
+    ctx = cp.Context(32, 4, 128, 8, 8013, 4096, v_cache_f16=True)
+    assert ctx.v_staging_bytes(num_seqs) == num_seqs * 4096 * 4 * 128 * 2
+    for bad in (0, 129):
+        with pytest.raises(cp.CpattnError) as e:
+            ctx.v_staging_bytes(bad)
+        assert e.value.status == cp.E_INVALID
+
+
+def test_v_staging_too_small_is_refused_before_launch(lib):
+    ctx = cp.Context(8, 2, 128, 4, 4000, 64, v_cache_f16=True)
+    need = ctx.v_staging_bytes(2)
+    assert ctx.lib.cpattn_set_v_staging(ctx._h, 4096, need - 16) == cp.OK
+    A = 256
+    st = ctx.prefill_raw([100, 7], [64, 5], A, A, A, A, A, A, None, stream=0)
+    assert st == cp.E_INVALID and "V staging buffer" in ctx.last_error()
+    # Enough for one sequence, not for two.
+    assert ctx.lib.cpattn_set_v_staging(ctx._h, 4096, ctx.v_staging_bytes(1)) == cp.OK
+    st = ctx.prefill_raw([100, 7], [64, 5], A, A, A, A, A, A, None, stream=0)
+    assert st == cp.E_INVALID and "V staging buffer" in ctx.last_error()
+
+
 def test_pingpong_plans_per_sm(lib):
     """Two query tiles per CTA: every SM is an executor of head pairs, so a
     short chunk against a long cache is cut into more pieces than for CTA

@@ -38,9 +38,10 @@ def _valid(w):
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["write_then_prefill", "fused_write"])
-@pytest.mark.parametrize("v_f16", [False, True], ids=["bf16_v", "f16_v"])
+@pytest.mark.parametrize("v_f16,staged", [(False, False), (True, False), (True, True)],
+                         ids=["bf16_v", "f16_v", "f16_v_staged"])
 @pytest.mark.parametrize("r", REQUESTS, ids=[r.name for r in REQUESTS])
-def test_cumulative_request(r, v_f16, fused):
+def test_cumulative_request(r, v_f16, staged, fused):
     steps = generate_request(r)
     shape = (r.num_seqs, r.num_kv_heads, r.shards, r.shard_capacity, r.head_dim)
     # Both sides start from the same caches (finite fill, the chunk rows
@@ -51,6 +52,10 @@ def test_cumulative_request(r, v_f16, fused):
     vc = Guarded(shape, vc_ref, dtype=torch.float16 if v_f16 else torch.bfloat16)
     ctx = cp.Context(r.num_q_heads, r.num_kv_heads, r.head_dim, r.shards, r.shard_capacity,
                      r.chunk, 0.0, False, v_f16)
+    if staged:  # the chunk's V staged in fp16: every tile takes fp16 P
+        stage = torch.empty(ctx.v_staging_bytes(r.num_seqs) // 2, dtype=torch.float16,
+                            device="cuda")
+        ctx.set_v_staging(stage)
     vconv = oracle.f16_bits_to_f64 if v_f16 else oracle.bits_to_f64
     for k, inp in enumerate(steps):
         w = r.step(k)
