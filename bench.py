@@ -673,6 +673,8 @@ def precision_label(fast_p: bool, v_f16: bool) -> str:
 
 
 def traffic_key(kname: str, workload: str, fast_p: bool, v_f16: bool) -> str:
+    if v_f16 and V_STAGING:  # every tile one fp16 product: fast_p does not apply
+        return f"{kname}:{workload}:vf16staged"
     return f"{kname}:{workload}:{'fast_p' if fast_p else 'accurate'}" + (":vf16" if v_f16 else "")
 
 
@@ -782,7 +784,9 @@ def main():
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "pinned host buffers; uploads and downloads on their own streams overlap the previous/next step's kernels"},
-        "gpu_launches": {"fused": 2, "two_launch": 4, "fused_write": 1}[args.variant] * args.steps,
+        # write_kv, the V staging (fp16 V cache), prefill.
+        "gpu_launches": ({"fused": 2, "two_launch": 4, "fused_write": 1}[args.variant]
+                         + (1 if v_f16 and V_STAGING else 0)) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_extras and world == 1:
