@@ -98,17 +98,25 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.first = 0
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # nvidia-smi takes a while to start: wait for its first sample so
+            # that a short timed region is sampled from its start; samples
+            # taken before the region are not counted.
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
+        self.first = len(self.lines)
         return self
 
     def _read(self):
@@ -117,6 +125,7 @@ class ClockSampler:
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.06)  # one more sample interval: the region's tail
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -126,7 +135,7 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in self.lines[self.first:]:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 8:
                 continue
