@@ -225,13 +225,21 @@ cpattn_status launch_prefill(cpattn_ctx* ctx, cpattn::PrefillParams* prm, cudaSt
   cfg.blockDim = dim3(cpattn::kThreads, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = MC ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if constexpr (VF16 == cpattn::kVF16All) {
+    // A programmatic dependent of the V staging kernel just launched on the
+    // stream: its prologue overlaps the staging, and its producer waits for
+    // the staging grid (griddep_wait) before the first copy.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *prm);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "prefill launch");
   return after_launch(ctx, stream, "prefill launch");
@@ -505,9 +513,12 @@ cpattn_status stage_v(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* chunk_le
   p.vec_per_row = c.head_dim * 2 / 16;
   p.total_vecs = static_cast<long long>(need / 16);
   for (int b = 0; b < num_seqs; ++b) p.chunk_len[b] = chunk_lens[b];
+  // One wave (4 blocks of 256 threads per SM, grid-stride beyond): every
+  // block starts at once, so the prefill kernel, its programmatic dependent,
+  // may launch as soon as the blocks have started.
   const long long blocks = (p.total_vecs + 255) / 256;
   const int grid =
-      static_cast<int>(std::min<long long>(blocks, static_cast<long long>(ctx->num_sms) * 16));
+      static_cast<int>(std::min<long long>(blocks, static_cast<long long>(ctx->num_sms) * 4));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cpattn::stage_v_f16_kernel<<<grid, 256, 0, st>>>(p);
   cpattn_status s = after_launch(ctx, st, "V staging launch");

@@ -355,7 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     if constexpr (Ly::SPLIT_O) reg_alloc_dec<kOtherRegs>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer_role_pair2<HD>(p, sbase, wait);
+      if (lane == 0) {
+        // The staged fp16 V is written by the kernel this one depends on.
+        if constexpr (VF16 == kVF16All) griddep_wait();
+        producer_role_pair2<HD>(p, sbase, wait);
+      }
     } else if (warp == kWriterWarp) {
       if (p.k_cache_w != nullptr) kv_write_lanes<HD, VF16 != kVBf16, 2>(p, lane);
     } else if (warp == kMmaWarp && rank == 0) {

@@ -492,7 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarp) {
     softmax_role_pingpong<SPLIT, VF16>(p, sbase, tmem, wait);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_role_pingpong(p, sbase, wait);
+    if (lane == 0) {
+      // The staged fp16 V is written by the kernel this one depends on.
+      if constexpr (VF16 == kVF16All) griddep_wait();
+      producer_role_pingpong(p, sbase, wait);
+    }
   } else if (warp == kWriterWarp) {
     if (p.k_cache_w != nullptr)
       kv_write_units<Ly::HD, VF16 != kVBf16>(p, lane,

@@ -183,6 +183,17 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return true;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the kernel ahead of it on the stream has
+// finished; griddep_wait blocks the calling thread until that grid has
+// completed and its writes are visible (immediately, when the launch was an
+// ordinary one).  griddep_launch_dependents lets the next kernel start once
+// every block of this grid has called it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Register reallocation between warpgroups (every warp of a warpgroup
 // executes the same one): .inc waits until the CTA's pool, which the launch
 // sized at threads x registers per thread, has that many free per thread --

@@ -85,6 +85,11 @@ struct StageVParams {
 };
 
 __global__ void __launch_bounds__(256) stage_v_f16_kernel(const __grid_constant__ StageVParams p) {
+  // The prefill kernel is launched as a programmatic dependent of this one:
+  // it may start now (its blocks then occupy no SM this grid still needs,
+  // since every block of this grid has started), and its producer waits for
+  // this grid's completion before its first copy.
+  griddep_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long per_token = static_cast<long long>(p.nkv) * p.vec_per_row;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
