@@ -126,9 +126,11 @@ constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 // first launch); at HD = 128 the two softmax warpgroups then take
 // kSoftmaxRegs and the third warpgroup keeps kOtherRegs -- exactly the
 // launch's pool, so the increase never waits for registers nobody frees.
+// 208 / 88 rather than 224 / 56: with 56 the MMA and producer roles spill,
+// with 200 the softmax does (varlen 3.75 ms at 224 / 56, 3.70 at 208 / 88).
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 224;
-constexpr int kOtherRegs = 56;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kOtherRegs = 88;
 static_assert(kThreads == 384 && kThreads * kLaunchRegs <= 65536, "one CTA per SM");
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs == kThreads * kLaunchRegs,
               "register split = launch allocation");
