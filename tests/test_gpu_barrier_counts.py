@@ -76,10 +76,14 @@ def _layout(form, hd):
     return nslot, per_tile, count
 
 
-def _run(w, mode, counted_lib, split_tiles=None, fused_write=False):
-    case = make_case(w)
+def _run(w, mode, counted_lib, split_tiles=None, fused_write=False, staged=False):
+    case = make_case(w, v_f16=staged)
     dc = DeviceCase(case)
-    ctx = cp.Context.for_workload(w, pairing=mode, library=counted_lib)
+    ctx = cp.Context.for_workload(w, pairing=mode, library=counted_lib, v_cache_f16=staged)
+    if staged:  # the chunk's V staged in fp16: the every-tile-fp16 kernel form
+        ctx._v_stage = torch.empty(ctx.v_staging_bytes(w.num_seqs) // 2, dtype=torch.float16,
+                                   device="cuda")
+        ctx.set_v_staging(ctx._v_stage)
     if split_tiles is not None:
         need, _ = ctx.splitkv_workspace(w.cache_lens, w.chunk_lens, split_tiles)
         ws = torch.empty(max(need // 4, 64), dtype=torch.float32, device="cuda")
@@ -214,6 +218,15 @@ def _check(w, mode, ctx, counts, totals=True):
 def test_barrier_counts_balance(w, mode, order, counted_lib, monkeypatch):
     monkeypatch.setenv("CPATTN_UNIT_ORDER", order)
     ctx, counts = _run(w, mode, counted_lib)
+    _check(w, mode, ctx, counts)
+
+
+@pytest.mark.parametrize("mode", ["mma2", "none", "pingpong"])
+@pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
+def test_barrier_counts_staged_v(w, mode, counted_lib):
+    """The every-tile-fp16 form (the chunk's V staged, its prefill a
+    programmatic dependent of the staging) keeps the same balance."""
+    ctx, counts = _run(w, mode, counted_lib, staged=True)
     _check(w, mode, ctx, counts)
 
 

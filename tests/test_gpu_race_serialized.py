@@ -5,7 +5,8 @@ producer/consumer hand-off in the pipeline; a protocol whose correctness
 depends on timing (e.g. an ambiguous mbarrier parity wait) fails here.  The
 selection spans every pipeline form: paired (2-SM MMA) and
 unpaired kernels, the two-query-tile kernel, split-KV pieces, GQA-packed units, the fused KV write, the
-fp16 V cache forms, and inputs that rescale O on every tile."""
+fp16 V cache forms (with and without the chunk's V staged in fp16, whose prefill starts as a
+programmatic dependent of the staging), and inputs that rescale O on every tile."""
 import os
 import subprocess
 import sys
