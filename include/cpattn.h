@@ -209,8 +209,9 @@ cpattn_status cpattn_prefill(cpattn_ctx* ctx, int32_t num_seqs, const int32_t* c
  * prefill never reads as keys.  Cache tiles at a shard's edge may load those
  * rows as masked columns, and they hold finite values before and after.
  * Arguments, layouts and errors are those of cpattn_prefill, with k_cache
- * and v_cache also written (in place); a registered split-KV workspace is
- * used as by cpattn_prefill.
+ * and v_cache also written (in place); a registered split-KV workspace and
+ * a registered V staging buffer are used as by cpattn_prefill (the staging
+ * kernel runs first; the writer warp still reads the bf16 v_new).
  */
 cpattn_status cpattn_prefill_write_kv(cpattn_ctx* ctx, int32_t num_seqs,
                                       const int32_t* cache_lens, const int32_t* chunk_lens,
@@ -227,7 +228,9 @@ cpattn_status cpattn_prefill_write_kv(cpattn_ctx* ctx, int32_t num_seqs,
  *   O = (e^{l1-m} O1 + e^{l2-m} O2) / (e^{l1-m} + e^{l2-m}),  m = max(l1, l2).
  * Same arguments and result as cpattn_prefill, plus a caller-owned device
  * workspace of at least cpattn_two_launch_workspace() bytes, 256-byte
- * aligned, used only during the call's kernels on `stream`.
+ * aligned, used only during the call's kernels on `stream`.  With a
+ * registered V staging buffer the chunk's V is staged once, before launch 1,
+ * and both launches take the fused launch's tile forms.
  * Errors: as cpattn_prefill; E_INVALID also for a small or misaligned workspace.
  */
 cpattn_status cpattn_two_launch_workspace(const cpattn_ctx* ctx, int32_t num_seqs,
