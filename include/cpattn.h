@@ -47,7 +47,8 @@ typedef enum {
   CPATTN_E_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
   CPATTN_E_NOMEM = 4,        /* host or device allocation failed (create only) */
   CPATTN_E_TIMEOUT = 5,      /* a device-side bounded wait expired; context still usable */
-  CPATTN_E_RANGE = 6         /* a value written to an fp16 V cache lies outside fp16's range */
+  CPATTN_E_RANGE = 6         /* a V value converted to fp16 (fp16 V cache or V staging)
+                                lies outside fp16's range */
 } cpattn_status;
 
 typedef struct {

@@ -703,7 +703,8 @@ cpattn_status cpattn_sync_status(cpattn_ctx* ctx, void* stream) {
                   "it returned without computing");
     if ((word & 0xFF) == cpattn::kStatusRange)
       return fail(ctx, CPATTN_E_RANGE,
-                  "a V value written to the fp16 V cache lies outside fp16's finite range");
+                  "a V value converted to fp16 (for the fp16 V cache, or staged) lies outside "
+                  "fp16's finite range");
     return fail(ctx, CPATTN_E_TIMEOUT,
                 "a bounded device wait expired (site " + std::to_string(word >> 8) + ")");
   }
