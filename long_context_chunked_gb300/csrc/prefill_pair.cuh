@@ -171,6 +171,12 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
   auto bar = [&](int i) { return sbase + Ly::OFF_BAR + 8u * static_cast<uint32_t>(i); };
   const uint32_t q_base = sbase + Ly::OFF_Q;
   const uint32_t ring = sbase + Ly::OFF_RING;
+  // Operand descriptors are a base's descriptor plus (offset >> 4): the
+  // start-address field holds address >> 4 in 14 bits, and every offset
+  // stays inside its buffer (Q, or one ring slot), so the sum never carries.
+  // Fewer instructions in the MMA warp, which shares a sub-partition with
+  // two softmax warps.
+  const uint64_t qdesc = make_sdesc_sw128(q_base, 16, 1024);
   RingPos rp;
   uint32_t tile_ctr = 0, units = 0;
   bool ok = true;
@@ -215,11 +221,12 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
       if (!wwait(bar(Ly::B_SLOTFULL + rp.slot), rp.phase, kSiteSlotFull)) return false;
       tc_fence_after();
       const uint32_t vb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
+      const uint64_t vdesc = make_sdesc_sw128(vb, Pl::VR * 128, 1024);
 #pragma unroll
       for (int kk = 0; kk < Pl::VR / 16; ++kk) {
         // V: VCH column chunks of VR rows x 128 B (chunk stride VR * 128),
         // 16 key rows per step.
-        const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, Pl::VR * 128, 1024);
+        const uint64_t bd = vdesc + static_cast<uint64_t>((kk * 2048) >> 4);
         const int e0 = j * Pl::VR + kk * 16;
         const uint32_t pa = p_tmem + 32 * (e0 >> 5) + ((e0 & 31) >> 1);
         if (F16) {
@@ -260,13 +267,14 @@ __device__ __forceinline__ void mma_role_pair2(const PrefillParams& p, uint32_t 
         }
         tc_fence_after();
         const uint32_t kb = ring + static_cast<uint32_t>(rp.slot) * Ly::SUB;
+        const uint64_t kdesc = make_sdesc_sw128(kb, 16, 1024);
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int c = 2 * j + c2;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = make_sdesc_sw128(q_base + c * (kBQ * 128) + kk * 32, 16, 1024);
-            const uint64_t bd = make_sdesc_sw128(kb + c2 * Pl::BOX + kk * 32, 16, 1024);
+            const uint64_t ad = qdesc + static_cast<uint64_t>((c * (kBQ * 128) + kk * 32) >> 4);
+            const uint64_t bd = kdesc + static_cast<uint64_t>((c2 * Pl::BOX + kk * 32) >> 4);
             mma2_ss(s_tmem, ad, bd, Pl::IDESC_QK, (c | kk) != 0);
           }
         }
