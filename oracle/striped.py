@@ -95,8 +95,10 @@ def bf16_bits(x) -> np.ndarray:
 
 
 def bits_to_f64(u16: np.ndarray) -> np.ndarray:
-    """Decode bf16 bit patterns (uint16) to float64 exactly."""
-    return (np.asarray(u16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    """Decode bf16 bit patterns (uint16) to float64 exactly (NaN patterns,
+    signalling ones included, decode to NaN without a floating-point warning)."""
+    with np.errstate(invalid="ignore"):
+        return (np.asarray(u16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def bf16_to_f16_bits(u16: np.ndarray) -> np.ndarray:
