@@ -330,6 +330,15 @@ def test_v_staging_too_small_is_refused_before_launch(lib):
     assert ctx.lib.cpattn_set_v_staging(ctx._h, 4096, ctx.v_staging_bytes(1)) == cp.OK
     st = ctx.prefill_raw([100, 7], [64, 5], A, A, A, A, A, A, None, stream=0)
     assert st == cp.E_INVALID and "V staging buffer" in ctx.last_error()
+    # The fused-write and two-launch entry points stage too, and refuse alike.
+    st = ctx.prefill_write_kv_raw([100, 7], [64, 5], A, A, A, A, A, A, None, stream=0)
+    assert st == cp.E_INVALID and "V staging buffer" in ctx.last_error()
+    cl, ch = (ctypes.c_int32 * 2)(100, 7), (ctypes.c_int32 * 2)(64, 5)
+    ws = ctypes.c_uint64()
+    assert ctx.lib.cpattn_two_launch_workspace(ctx._h, 2, ctypes.byref(ws)) == cp.OK
+    st = ctx.lib.cpattn_prefill_two_launch(ctx._h, 2, cl, ch, A, A, A, A, A, A, None, 4096,
+                                           ws.value, None)
+    assert st == cp.E_INVALID and "V staging buffer" in ctx.last_error()
 
 
 def test_pingpong_plans_per_sm(lib):
