@@ -777,6 +777,7 @@ def main():
         "config": {"workload": w.name, "description": w.description,
                    "precision": precision_label(args.fast_p, v_f16),
                    "v_cache": args.v_cache,
+                   "v_staging": bool(v_f16 and V_STAGING),
                    "l2": "flushed between steps (512 MiB write)",
                    "parallelism": f"replicas x{world}", "variant": args.variant},
         "prefill_ms": round(pf, 4), "write_kv_ms": round(kv_ms, 4),
