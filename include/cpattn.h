@@ -265,7 +265,7 @@ cpattn_status cpattn_prefill_two_launch(cpattn_ctx* ctx, int32_t num_seqs,
  *   max_split_tiles  0: automatic -- a cost model of the persistent grid
  *                    (units handed out cyclically, longest first, each
  *                    costing its tiles plus a fixed fill/drain) picks, among
- *                    pieces of ceil(n_max / k) tiles (k = 2..64, at least 16
+ *                    pieces of ceil(n_max / k) tiles (k = 2..64, at least 8
  *                    tiles), the cut with the lowest modelled makespan, and
  *                    cuts only if that beats the unsplit plan by 10 %;
  *                    > 0: every walk longer than this many tiles is cut into
